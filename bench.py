@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Prefill throughput of the gated delta rule forward pass (chunk-parallel WY
+form) on GB300, with its roofline and the fp64 oracle timed on the host cores.
+
+One step = one pass of the whole hot path (chunk-prep kernel + scan kernel)
+over one batch of synthetic input.  Default workload: the 32k-token spot of
+stratat pull #1296 ("Measured verdict on gfx1100": 32k tokens, HV = 48 value
+heads, state 128) as bf16 GDN with 16 q/k heads and chunk 64.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  Multi-GPU (torchrun, one rank per GPU): every
+rank runs its own copy of the workload (independent sequences, no collective
+on the data path) -> weak scaling; the value is all ranks' tokens over the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s (gated delta-rule fwd, 1 GB300) and % of HBM/tensor roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "gdn_bf16_t32768"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workload arithmetic (per-token bytes and FLOPs of the roofline)
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(c, which="path"):
+    """HBM bytes each kernel must move at least once: q, k, v, g, beta read,
+    o written (states excluded, <= ~1% here)."""
+    es = 2 if c.dtype_name == "bf16" else 4
+    n = c.tokens
+    qk = 2 * n * c.H * c.dk * es
+    vo = 2 * n * c.HV * c.dv * es
+    gb = n * c.HV * (1 if c.gate_mode == 0 else c.dk) * 4
+    bb = n * c.HV * 4
+    if which == "prep":  # reads q, k, g, beta
+        return qk + gb + bb
+    return qk + vo + gb + bb  # scan and whole path: everything once
+
+
+def algorithmic_flops(c):
+    """Chunk-GEMM FLOPs, dense count: per token and value head
+    2 (3 C dk + 2 C dv + 3 dk dv): Gram, W, Aqk; U, O_intra; W S, Qg S, Kt^T Vn."""
+    C, dk, dv = c.chunk, c.dk, c.dv
+    return c.tokens * c.HV * 2 * (3 * C * dk + 2 * C * dv + 3 * dk * dv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunkwise_gated_delta_gdn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload, kernel, units):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; scaled by units processed when the capture
+    ran a smaller case."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None, None
+    for e in rec.get("entries", []):
+        if e.get("kernel") == kernel and e.get("source_sha") == kernel_source_sha():
+            per_unit = float(e["dram_bytes"]) / float(e["tokens"])
+            return per_unit * units, e.get("note")
+    return None, None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU side: the oracle
+# ---------------------------------------------------------------------------
+def oracle_sample(c, x, n_tokens):
+    """Run the token-serial oracle on the first n_tokens of every sequence
+    row (all value heads); returns (seconds, tokens processed)."""
+    import numpy as np
+    import oracle
+
+    Bq = x["q"].shape[0]
+    n_tokens = max(1, min(n_tokens, x["q"].shape[1]))
+    if x["cu_seqlens"] is not None:  # packed: the first sequence's prefix
+        first = int(x["cu_seqlens"][1])
+        n_tokens = min(n_tokens, first)
+        Bq = 1
+    q = x["q"][:Bq, :n_tokens].reshape(-1, c.H, c.dk)
+    k = x["k"][:Bq, :n_tokens].reshape(-1, c.H, c.dk)
+    v = x["v"][:Bq, :n_tokens].reshape(-1, c.HV, c.dv)
+    g = x["g"][:Bq, :n_tokens].reshape((-1,) + tuple(x["g"].shape[2:]))
+    beta = x["beta"][:Bq, :n_tokens].reshape(-1, c.HV)
+    h0 = x["h0"][:Bq] if x["h0"] is not None else None
+    cu = np.arange(Bq + 1, dtype=np.int64) * n_tokens
+    t = time.perf_counter()
+    oracle.token_serial(q, k, v, g, beta, h0, cu, c.scale, c.gate_mode)
+    return time.perf_counter() - t, Bq * n_tokens
+
+
+def calibrate_oracle(c, x, target_s):
+    sec, n = oracle_sample(c, x, 64)
+    per_token = sec / n
+    return max(16, int(target_s / max(per_token, 1e-9)))
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.gpus > 1 and world == 1:
+        raise SystemExit("--gpus N > 1 must be launched with torchrun (one rank per GPU)")
+
+    from chunkwise_gated_delta_gdn_gb300 import synth
+
+    c0 = synth.case(args.workload)
+
+    class W:  # workload view with the fields the arithmetic needs
+        pass
+
+    wl = W()
+    for f in ("H", "HV", "dk", "dv", "chunk", "gate_mode", "scale"):
+        setattr(wl, f, getattr(c0, f))
+    wl.tokens = c0.tokens
+    wl.dtype_name = "bf16" if str(c0.dtype).endswith("bfloat16") else "f32"
+    config = {"workload": c0.name, "B": c0.B, "T": c0.T, "H": c0.H, "HV": c0.HV,
+              "dk": c0.dk, "dv": c0.dv, "chunk": c0.chunk,
+              "gate": "scalar (GDN)" if c0.gate_mode == 0 else "per-key (KDA)",
+              "n_seqs": c0.num_states, "h0": c0.h0_std is not None}
+
+    if args.impl == "reference":
+        run_reference(args, rank, world, c0, wl, config)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    from chunkwise_gated_delta_gdn_gb300 import build as cuda_build
+    from chunkwise_gated_delta_gdn_gb300 import gdn
+
+    gdn.load(cuda_build.build())
+    x = synth.make_inputs(c0)
+    names = ("q", "k", "v", "g", "beta", "h0", "cu_seqlens")
+    d = {n: (x[n].to(dev) if x[n] is not None else None) for n in names}
+    B, T = x["q"].shape[0], x["q"].shape[1]
+    n_states = c0.num_states
+    o = torch.empty((B, T, c0.HV, c0.dv), dtype=c0.dtype, device=dev)
+    hT = torch.empty((n_states, c0.HV, c0.dk, c0.dv), dtype=torch.float32, device=dev)
+    dt = gdn.GDN_BF16 if c0.dtype == torch.bfloat16 else gdn.GDN_F32
+    ws_bytes = gdn.gdn_chunk_fwd_workspace_bytes(B, T, c0.H, c0.HV, c0.dk, c0.dv, c0.chunk,
+                                                 c0.gate_mode, n_states, dt)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    kw = dict(workspace=ws, o=o, hT=hT, scale=c0.scale, chunk=c0.chunk,
+              cu_seqlens=d["cu_seqlens"])
+    args_in = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+
+    def step():
+        gdn.gdn_chunk_fwd_prep(*args_in, **kw)
+        gdn.gdn_chunk_fwd_scan(*args_in, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flags = gdn.gdn_read_device_flags(ws)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.25)  # let the sampler come up before the timed region
+    ev_start.record()
+    for i in range(K):
+        ev[i][0].record()
+        gdn.gdn_chunk_fwd_prep(*args_in, **kw)
+        ev[i][1].record()
+        gdn.gdn_chunk_fwd_scan(*args_in, **kw)
+        ev[i][2].record()
+    ev_end.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = ev_start.elapsed_time(ev_end)
+    prep_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    scan_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    ms_step = ms_total / K
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    tokens_per_rank = c0.tokens
+    value = world * tokens_per_rank / (ms_step / 1e3)
+
+    # ---- end to end through the public binding, host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        host = {n: (x[n].pin_memory() if x[n] is not None else None) for n in names}
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        h_host = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names if host[n] is not None)
+        d2h = o_host.numel() * o_host.element_size() + h_host.numel() * h_host.element_size()
+
+        def e2e_step():
+            for n in names:
+                if host[n] is not None:
+                    d[n].copy_(host[n], non_blocking=True)
+            gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o=o, hT=hT,
+                              workspace=ws, scale=c0.scale, chunk=c0.chunk,
+                              cu_seqlens=d["cu_seqlens"])
+            o_host.copy_(o, non_blocking=True)
+            h_host.copy_(hT, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * tokens_per_rank / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms, "steps": args.e2e_steps}
+
+    # ---- roofline ----
+    peaks, peak_src = load_peaks()
+    dominant = "scan" if scan_ms >= prep_ms else "prep"
+    kern_ms = scan_ms if dominant == "scan" else prep_ms
+    kbytes = algorithmic_bytes(wl, dominant)
+    achieved = kbytes / (kern_ms / 1e3) / 1e9
+    traffic, traffic_note = measured_traffic(c0.name, dominant, c0.tokens)
+    roofline = {"bound": "hbm", "kernel": f"gdn_{dominant}_kernel", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": traffic, "algorithmic_bytes": kbytes, "kernel_ms": kern_ms,
+                "peak_source": f"hbm_gbs of {peak_src}"}
+    if traffic_note:
+        roofline["traffic_note"] = traffic_note
+    path_bytes = algorithmic_bytes(wl, "path")
+    path_flops = algorithmic_flops(wl)
+    t_hbm = path_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = path_flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    path = {"bytes": path_bytes, "flops": path_flops, "t_hbm_us": t_hbm * 1e6,
+            "t_tensor_us": t_tc * 1e6, "bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "frac": max(t_hbm, t_tc) / (ms_step / 1e3 / world) if ms_step > 0 else None,
+            "note": f"whole path vs max(HBM, tensor) roofline of {peak_src} peaks"}
+
+    # ---- CPU baseline (oracle) on rank 0 at N = 1 ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n_tok = calibrate_oracle(wl, x, args.cpu_seconds)
+        sec, n = oracle_sample(wl, x, n_tok)
+        cpu = {"value": n / sec, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"fp64 token-serial oracle on the first {n} tokens (all {c0.HV} value "
+                         f"heads) of {c0.name}, {sec:.1f} s"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype_name,
+            "data": "synthetic (seeded; no dataset)",
+            "config": dict(config, l2="inputs 1 GB+ and workspace exceed the 129 MB L2; no flush",
+                           parallelism=f"replicas x{world}"),
+            "roofline": roofline, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": 2 * K,
+            "kernels_ms": {"prep": prep_ms, "scan": scan_ms}, "device_flags": flags}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args, rank, world, c0, wl, config):
+    """The oracle as it stands, timed on the host cores (the reference arm)."""
+    if rank != 0:
+        return
+    import oracle
+    from chunkwise_gated_delta_gdn_gb300 import synth
+
+    x = synth.make_inputs(c0)
+    total = args.steps + args.warmup
+    per_step_s = min(10.0, 150.0 / max(total, 1))
+    n_tok = calibrate_oracle(wl, x, per_step_s)
+    for _ in range(args.warmup):
+        oracle_sample(wl, x, n_tok)
+    times, n = [], 0
+    for _ in range(args.steps):
+        sec, n = oracle_sample(wl, x, n_tok)
+        times.append(sec)
+    ms_step = 1e3 * sum(times) / len(times)
+    value = n / (ms_step / 1e3)
+    cores = oracle.num_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; no dataset)",
+            "config": config,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: fp64 token-serial oracle on the first {n} "
+                                       f"tokens (all {c0.HV} value heads) of {c0.name}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+// gdn_api.cu -- host side of the C ABI declared in include/gdn.h: argument
+// validation, workspace sizing and the two launches (prep, then scan) on the
+// caller's stream.  Unsupported requests are refused explicitly, before
+// anything is enqueued (logismos issue #46, "Acceptance": unsupported inputs
+// fail explicitly).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cmath>
+#include <cstddef>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+struct Plan {
+  int n_states;   // B, or n_seqs when packed
+  long Ttot;      // packed token count
+  long n_slots;   // chunk slots of the workspace
+  size_t tile_bytes;
+  size_t ws_bytes;
+};
+
+// Shape checks shared by the workspace query and the call.  Returns GDN_OK
+// and fills `p`, or the status the call must return.
+gdn_status plan(int B, int T, int H, int HV, int dk, int dv, int chunk,
+                int gate_mode, int n_seqs, int dtype, bool packed, Plan &p) {
+  if (B <= 0 || T < 0 || H <= 0 || HV <= 0 || dk <= 0 || dv <= 0 || chunk <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (HV % H != 0 || HV > 65535) return GDN_ERR_INVALID_ARG;
+  if (gate_mode != GDN_GATE_SCALAR && gate_mode != GDN_GATE_PER_KEY) return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (packed) {
+    if (B != 1 || n_seqs <= 0) return GDN_ERR_INVALID_ARG;
+    p.n_states = n_seqs;
+  } else {
+    if (n_seqs != 0 && n_seqs != B) return GDN_ERR_INVALID_ARG;
+    p.n_states = B;
+  }
+  if (!(dk == 64 || dk == 128) || !(dv == 64 || dv == 128)) return GDN_ERR_UNSUPPORTED;
+  if (!(chunk == 32 || chunk == 64)) return GDN_ERR_UNSUPPORTED;
+  p.Ttot = (long)B * T;
+  if (p.Ttot > INT32_MAX - 2L * chunk) return GDN_ERR_UNSUPPORTED;
+  p.n_slots = p.Ttot / chunk + p.n_states;
+  if (p.n_slots > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+  p.tile_bytes = (size_t)p.n_slots * (size_t)HV * 2u * (size_t)chunk * (size_t)chunk * sizeof(float);
+  p.ws_bytes = gdn::kWorkspaceHeader + p.tile_bytes;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_version(void) { return 100; }
+
+const char *gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    default: return "GDN_ERR_UNKNOWN";
+  }
+}
+
+size_t gdn_chunk_fwd_workspace_bytes(int B, int T, int H, int HV, int dk, int dv,
+                                     int chunk, int gate_mode, int n_seqs, int dtype) {
+  Plan p;
+  // a packed request is one with B == 1 and n_seqs > 1, or n_seqs given with B == 1;
+  // the size only depends on the number of states, so both readings agree
+  const bool packed = (B == 1 && n_seqs > 1);
+  if (plan(B, T, H, HV, dk, dv, chunk, gate_mode, n_seqs, dtype, packed, p) != GDN_OK) return 0;
+  return p.ws_bytes;
+}
+
+}  // extern "C"
+
+namespace {
+
+enum Stage { kPrep = 1, kScan = 2, kBoth = 3 };
+
+gdn_status run(int stages, const void *q, const void *k, const void *v, const float *g,
+               const float *beta, const float *h0, void *o, float *hT,
+               const int32_t *cu_seqlens, int n_seqs, int B, int T, int H, int HV, int dk,
+               int dv, int chunk, float scale, int gate_mode, int dtype, void *workspace,
+               size_t workspace_bytes, gdn_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const bool packed = cu_seqlens != nullptr;
+  Plan p;
+  gdn_status st = plan(B, T, H, HV, dk, dv, chunk, gate_mode, n_seqs, dtype, packed, p);
+  if (st != GDN_OK) return st;
+  if (!std::isfinite(scale)) return GDN_ERR_INVALID_ARG;
+
+  // pointers: required ones non-null (token data may be absent when there are
+  // no tokens), all 16-byte aligned
+  if (p.Ttot > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, g, beta, h0, o, hT, cu_seqlens, workspace};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < p.ws_bytes) return GDN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_INVALID_ARG;
+
+  // aliasing: hT vs h0; o and hT vs every input; workspace vs everything
+  const size_t es = dtype == GDN_BF16 ? 2 : 4;
+  const size_t n_qk = (size_t)p.Ttot * H * dk * es;
+  const size_t n_vo = (size_t)p.Ttot * HV * dv * es;
+  const size_t n_g = (size_t)p.Ttot * HV * (gate_mode == GDN_GATE_PER_KEY ? dk : 1) * 4;
+  const size_t n_b = (size_t)p.Ttot * HV * 4;
+  const size_t n_h = (size_t)p.n_states * HV * dk * dv * 4;
+  if (overlap(hT, n_h, h0, n_h)) return GDN_ERR_INVALID_ARG;
+  const void *ins[] = {q, k, v, g, beta, h0};
+  const size_t in_n[] = {n_qk, n_qk, n_vo, n_g, n_b, n_h};
+  for (int i = 0; i < 6; i++) {
+    if (overlap(o, n_vo, ins[i], in_n[i])) return GDN_ERR_INVALID_ARG;
+    if (overlap(hT, n_h, ins[i], in_n[i])) return GDN_ERR_INVALID_ARG;
+    if (overlap(workspace, p.ws_bytes, ins[i], in_n[i])) return GDN_ERR_INVALID_ARG;
+  }
+  if (overlap(o, n_vo, hT, n_h) || overlap(workspace, p.ws_bytes, o, n_vo) ||
+      overlap(workspace, p.ws_bytes, hT, n_h))
+    return GDN_ERR_INVALID_ARG;
+
+  uint32_t *flags = static_cast<uint32_t *>(workspace);
+  gdn::SeqInfo seq;
+  seq.cu = cu_seqlens;
+  seq.n_seqs = p.n_states;
+  seq.T = T;
+  seq.Ttot = (int)p.Ttot;
+  float *tiles = reinterpret_cast<float *>(static_cast<char *>(workspace) + gdn::kWorkspaceHeader);
+
+  if (stages & kPrep) {
+    if (cudaMemsetAsync(flags, 0, sizeof(uint32_t), stream) != cudaSuccess) return GDN_ERR_CUDA;
+    if (p.Ttot > 0) {
+      gdn::PrepArgs pa;
+      pa.q = q; pa.k = k; pa.g = g; pa.beta = beta;
+      pa.seq = seq; pa.H = H; pa.HV = HV; pa.scale = scale;
+      pa.tiles = tiles; pa.flags = flags; pa.n_slots = (int)p.n_slots;
+      if (gdn::launch_prep(pa, chunk, dk, dtype, gate_mode, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    }
+  }
+  if (stages & kScan) {
+    gdn::ScanArgs sa;
+    sa.q = q; sa.k = k; sa.v = v; sa.g = g; sa.beta = beta; sa.h0 = h0;
+    sa.o = o; sa.hT = hT; sa.seq = seq; sa.H = H; sa.HV = HV; sa.dv = dv;
+    sa.scale = scale; sa.tiles = tiles; sa.flags = flags;
+    if (gdn::launch_scan(sa, chunk, dk, dtype, gate_mode, stream) != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, const float *h0, void *o, float *hT,
+                         const int32_t *cu_seqlens, int n_seqs, int B, int T, int H,
+                         int HV, int dk, int dv, int chunk, float scale, int gate_mode,
+                         int dtype, void *workspace, size_t workspace_bytes,
+                         gdn_stream_t stream) {
+  return run(kBoth, q, k, v, g, beta, h0, o, hT, cu_seqlens, n_seqs, B, T, H, HV, dk, dv,
+             chunk, scale, gate_mode, dtype, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_chunk_fwd_prep(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, const float *h0, void *o, float *hT,
+                              const int32_t *cu_seqlens, int n_seqs, int B, int T, int H,
+                              int HV, int dk, int dv, int chunk, float scale, int gate_mode,
+                              int dtype, void *workspace, size_t workspace_bytes,
+                              gdn_stream_t stream) {
+  return run(kPrep, q, k, v, g, beta, h0, o, hT, cu_seqlens, n_seqs, B, T, H, HV, dk, dv,
+             chunk, scale, gate_mode, dtype, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_chunk_fwd_scan(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, const float *h0, void *o, float *hT,
+                              const int32_t *cu_seqlens, int n_seqs, int B, int T, int H,
+                              int HV, int dk, int dv, int chunk, float scale, int gate_mode,
+                              int dtype, void *workspace, size_t workspace_bytes,
+                              gdn_stream_t stream) {
+  return run(kScan, q, k, v, g, beta, h0, o, hT, cu_seqlens, n_seqs, B, T, H, HV, dk, dv,
+             chunk, scale, gate_mode, dtype, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_read_device_flags(const void *workspace, uint32_t *flags_out,
+                                 gdn_stream_t stream_) {
+  if (!workspace || !flags_out) return GDN_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
+  *flags_out = v;
+  return GDN_OK;
+}
+
+}  // extern "C"

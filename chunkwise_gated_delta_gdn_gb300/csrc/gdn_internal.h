@@ -1,0 +1,60 @@
+// gdn_internal.h -- declarations shared by the host API (gdn_api.cu) and the
+// kernel translation units (gdn_prep.cu, gdn_scan.cu).  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Bytes at the start of the workspace reserved for the device status word.
+constexpr size_t kWorkspaceHeader = 256;
+// Width of one dv slice handled by a scan CTA.
+constexpr int kScanSlice = 32;
+
+// Where packed sequence n starts: cu_seqlens[n], or n*T for plain batches.
+// Sequence n owns the chunk slots [floor(start_n / C) + n, ...): one slot per
+// chunk, injective over all sequences, fewer than floor(Ttot / C) + n_seqs.
+struct SeqInfo {
+  const int32_t *cu;  // device, or nullptr for a plain batch
+  int n_seqs;         // sequences (B for a plain batch)
+  int T;              // tokens per batch row (plain batch only)
+  int Ttot;           // packed token count
+};
+
+struct PrepArgs {
+  const void *q, *k;
+  const float *g, *beta;
+  SeqInfo seq;
+  int H, HV;
+  float scale;
+  float *tiles;      // [n_slots][HV][2][C][C]: T = (I+A)^-1, then Aqk
+  uint32_t *flags;   // device status word
+  int n_slots;
+};
+
+struct ScanArgs {
+  const void *q, *k, *v;
+  const float *g, *beta, *h0;
+  void *o;
+  float *hT;
+  SeqInfo seq;
+  int H, HV, dv;
+  float scale;
+  const float *tiles;
+  uint32_t *flags;
+};
+
+// Status-word bits (same values as GDN_FLAG_* in include/gdn.h).
+constexpr uint32_t kFlagPositiveGate = 1u << 0;
+constexpr uint32_t kFlagNonfinite = 1u << 1;
+constexpr uint32_t kFlagBadSeqlens = 1u << 2;
+
+// Launchers; return cudaErrorInvalidValue for an uncompiled combination.
+// dtype: 0 = fp32, 1 = bf16.  gate: 0 = scalar (GDN), 1 = per key (KDA).
+cudaError_t launch_prep(const PrepArgs &a, int chunk, int dk, int dtype,
+                        int gate, cudaStream_t stream);
+cudaError_t launch_scan(const ScanArgs &a, int chunk, int dk, int dtype,
+                        int gate, cudaStream_t stream);
+
+}  // namespace gdn

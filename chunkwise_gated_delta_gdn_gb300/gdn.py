@@ -1,0 +1,207 @@
+"""Thin ctypes binding of libgdn (``include/gdn.h``), same names as the C ABI.
+
+This module only marshals arguments: it checks tensor shapes, dtypes and
+devices, allocates outputs and the workspace through PyTorch when the caller
+does not pass them, and hands raw device pointers and the current CUDA stream
+to the library.  Every step of the computation runs in the library's CUDA
+kernels; there is no fallback.  If ``libgdn.so`` has not been built the first
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = 1
+GDN_ERR_UNSUPPORTED = 2
+GDN_ERR_WORKSPACE = 3
+GDN_ERR_CUDA = 4
+
+GDN_GATE_SCALAR = 0
+GDN_GATE_PER_KEY = 1
+GDN_F32 = 0
+GDN_BF16 = 1
+
+GDN_FLAG_POSITIVE_GATE = 1 << 0
+GDN_FLAG_NONFINITE = 1 << 1
+GDN_FLAG_BAD_SEQLENS = 1 << 2
+
+# every symbol include/gdn.h declares
+EXPORTED = ("gdn_version", "gdn_status_string", "gdn_chunk_fwd_workspace_bytes",
+            "gdn_chunk_fwd", "gdn_chunk_fwd_prep", "gdn_chunk_fwd_scan",
+            "gdn_read_device_flags")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, what: str = "gdn_chunk_fwd"):
+        self.status = status
+        super().__init__(f"{what}: {gdn_status_string(status)} ({status})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None):
+    """Load libgdn.so (it must have been built; see ``build.py``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libgdn.so not found at {path}: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        vp, sz, i32, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+        lib.gdn_version.argtypes = []
+        lib.gdn_version.restype = i32
+        lib.gdn_status_string.argtypes = [i32]
+        lib.gdn_status_string.restype = ctypes.c_char_p
+        lib.gdn_chunk_fwd_workspace_bytes.argtypes = [i32] * 10
+        lib.gdn_chunk_fwd_workspace_bytes.restype = sz
+        for name in ("gdn_chunk_fwd", "gdn_chunk_fwd_prep", "gdn_chunk_fwd_scan"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                           i32, i32, i32, i32, i32, f32, i32, i32, vp, sz, vp]
+            fn.restype = i32
+        lib.gdn_read_device_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+        lib.gdn_read_device_flags.restype = i32
+        _lib = lib
+    return _lib
+
+
+def gdn_version() -> int:
+    return int(load().gdn_version())
+
+
+def gdn_status_string(status: int) -> str:
+    return load().gdn_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return GDN_BF16
+    if t == torch.float32:
+        return GDN_F32
+    raise TypeError(f"unsupported q/k/v dtype {t}")
+
+
+def gdn_chunk_fwd_workspace_bytes(B: int, T: int, H: int, HV: int, dk: int, dv: int,
+                                  chunk: int, gate_mode: int, n_seqs: int,
+                                  dtype: int) -> int:
+    return int(load().gdn_chunk_fwd_workspace_bytes(B, T, H, HV, dk, dv, chunk,
+                                                     gate_mode, n_seqs, dtype))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _call(entry: str, q, k, v, g, beta, h0, scale, chunk, cu_seqlens, o, hT,
+          output_final_state, workspace, stream):
+    lib = load()
+    B, T, H, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    if k.shape != q.shape or v.shape[:2] != (B, T) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v: inconsistent shapes or dtypes")
+    if g.dim() == 3:
+        gate_mode = GDN_GATE_SCALAR
+    elif g.dim() == 4:
+        gate_mode = GDN_GATE_PER_KEY
+    else:
+        raise ValueError("g must be [B,T,HV] or [B,T,HV,dk]")
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("h0", h0),
+                    ("cu_seqlens", cu_seqlens), ("o", o), ("hT", hT),
+                    ("workspace", workspace)):
+        if t is not None and (t.device != dev or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous tensor on {dev}")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    if h0 is not None and h0.dtype != torch.float32:
+        raise TypeError("h0 must be float32")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    n_seqs = int(cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    dt = _dtype_code(q.dtype)
+    if scale is None:
+        scale = dk ** -0.5
+    if o is None:
+        o = torch.empty((B, T, HV, dv), dtype=q.dtype, device=dev)
+    if hT is None and output_final_state:
+        hT = torch.empty((n_seqs, HV, dk, dv), dtype=torch.float32, device=dev)
+    nbytes = gdn_chunk_fwd_workspace_bytes(B, T, H, HV, dk, dv, chunk, gate_mode, n_seqs, dt)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    status = getattr(lib, entry)(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(hT),
+        _ptr(cu_seqlens), n_seqs, B, T, H, HV, dk, dv, int(chunk), float(scale),
+        gate_mode, dt, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        ctypes.c_void_p(stream.cuda_stream))
+    if status != GDN_OK:
+        raise GdnError(status, entry)
+    return o, hT
+
+
+def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                  beta: torch.Tensor, h0: Optional[torch.Tensor] = None, *,
+                  scale: Optional[float] = None, chunk: int = 64,
+                  cu_seqlens: Optional[torch.Tensor] = None,
+                  o: Optional[torch.Tensor] = None, hT: Optional[torch.Tensor] = None,
+                  output_final_state: bool = True,
+                  workspace: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None
+                  ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Run the forward pass; returns ``(o, hT)`` (``hT`` None when not asked).
+
+    q, k ``[B, T, H, dk]``; v ``[B, T, HV, dv]`` (bf16 or fp32, same dtype);
+    g ``[B, T, HV]`` (scalar gate) or ``[B, T, HV, dk]`` (per-key gate), fp32;
+    beta ``[B, T, HV]`` fp32; h0 ``[N, HV, dk, dv]`` fp32 or None;
+    cu_seqlens int32 ``[N + 1]`` on the device for packed input (B == 1).
+    """
+    return _call("gdn_chunk_fwd", q, k, v, g, beta, h0, scale, chunk, cu_seqlens, o, hT,
+                 output_final_state, workspace, stream)
+
+
+def gdn_chunk_fwd_prep(q, k, v, g, beta, h0=None, *, workspace: torch.Tensor,
+                       o: torch.Tensor, hT: Optional[torch.Tensor] = None, scale=None,
+                       chunk: int = 64, cu_seqlens=None, stream=None) -> None:
+    """First half of gdn_chunk_fwd: the chunk-prep kernel (fills ``workspace``)."""
+    _call("gdn_chunk_fwd_prep", q, k, v, g, beta, h0, scale, chunk, cu_seqlens, o, hT,
+          hT is not None, workspace, stream)
+
+
+def gdn_chunk_fwd_scan(q, k, v, g, beta, h0=None, *, workspace: torch.Tensor,
+                       o: torch.Tensor, hT: Optional[torch.Tensor] = None, scale=None,
+                       chunk: int = 64, cu_seqlens=None, stream=None) -> None:
+    """Second half of gdn_chunk_fwd: the scan kernel (reads ``workspace``)."""
+    _call("gdn_chunk_fwd_scan", q, k, v, g, beta, h0, scale, chunk, cu_seqlens, o, hT,
+          hT is not None, workspace, stream)
+
+
+def gdn_read_device_flags(workspace: torch.Tensor,
+                          stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Status word (GDN_FLAG_*) of the last call that used ``workspace``."""
+    lib = load()
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    out = ctypes.c_uint32(0)
+    status = lib.gdn_read_device_flags(_ptr(workspace), ctypes.byref(out),
+                                       ctypes.c_void_p(stream.cuda_stream))
+    if status != GDN_OK:
+        raise GdnError(status, "gdn_read_device_flags")
+    return int(out.value)

@@ -1,0 +1,181 @@
+/*
+ * gdn.h -- C ABI of libgdn: the chunk-parallel (WY form) forward pass of the
+ * gated delta rule, GDN and KDA, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (stratat pull #1296, "What this is": the gated-delta-net
+ * recurrence rewritten in the chunk-parallel WY form; ROCm/rocm-libraries
+ * PR #11223, "Summary": KDA prefill with six state-independent tiles plus a
+ * serial state recurrence).  For every sequence and value head hv, with the
+ * fp32 state S (dk x dv, K-first: row = key channel, logismos issue #46
+ * "Verified implementation boundary") and t = 1..L:
+ *
+ *     S_t = diag(a_t) S_{t-1} + beta_t k_t (v_t - (diag(a_t) S_{t-1})^T k_t)^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * with a_t = exp(g_t): natural-log decay (issue #46, Sep 8 comment), one
+ * scalar per (token, value head) for GDN, one per key channel for KDA.  The
+ * value head hv reads q/k head hv / (HV / H) (grouped heads, same comment).
+ * The input state h0 is never written; the final state goes to a separate
+ * buffer hT (issue #46: immutable input state, separate output/next-state).
+ *
+ * Inside, the work is split in two kernels launched back to back on the
+ * caller's stream: a state-independent chunk-prep kernel, parallel over all
+ * (chunk, value head), and a scan kernel, serial over the chunks of each
+ * sequence and parallel over (sequence, value head, dv slice) (the split
+ * composition of PR #11223, "Summary").  The prep kernel's tiles cross to the
+ * scan kernel through the caller's workspace.
+ *
+ * Conventions common to every entry point
+ *  - Every pointer argument except `flags_out` is a DEVICE pointer.
+ *  - Ownership: the caller allocates every buffer, workspace included; the
+ *    library allocates no memory, keeps no per-call state and may be called
+ *    from several host threads at once (one-time kernel attribute set-up is
+ *    guarded internally).
+ *  - Asynchrony: work is enqueued on `stream` (NULL = legacy default stream)
+ *    and the call returns without synchronising.  Errors of the launch itself
+ *    are returned as GDN_ERR_CUDA; faults during execution surface at the
+ *    caller's next synchronisation.
+ *  - Errors: all argument checks run before anything is enqueued; a call that
+ *    returns anything but GDN_OK has enqueued nothing and written nothing.
+ *    Nothing aborts, throws or prints across the ABI.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that callers need no CUDA
+ * headers. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, aliasing */
+  GDN_ERR_UNSUPPORTED = 2, /* a valid request outside the compiled domain */
+  GDN_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+  GDN_ERR_CUDA = 4         /* the CUDA runtime refused a launch or attribute */
+} gdn_status;
+
+typedef enum gdn_gate_mode {
+  GDN_GATE_SCALAR = 0,  /* GDN: g is [.., HV], one log-gate per value head */
+  GDN_GATE_PER_KEY = 1  /* KDA: g is [.., HV, dk], one per key channel */
+} gdn_gate_mode;
+
+typedef enum gdn_dtype {
+  GDN_F32 = 0,  /* q, k, v, o are float32 */
+  GDN_BF16 = 1  /* q, k, v, o are bfloat16 */
+} gdn_dtype;
+
+/* Bits of the device status word kept in the first bytes of the workspace. */
+enum {
+  GDN_FLAG_POSITIVE_GATE = 1u << 0, /* some log-gate g > 0 (a decay above 1) */
+  GDN_FLAG_NONFINITE = 1u << 1,     /* a non-finite value was written to o/hT */
+  GDN_FLAG_BAD_SEQLENS = 1u << 2    /* cu_seqlens not 0 = c0 <= c1 <= .. = T;
+                                       affected sequences were skipped */
+};
+
+/* Library version, major*10000 + minor*100 + patch. */
+GDN_API int gdn_version(void);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+GDN_API const char *gdn_status_string(int status);
+
+/*
+ * Bytes of workspace gdn_chunk_fwd needs for this problem; 0 for a request
+ * that gdn_chunk_fwd would reject.  Arguments as for gdn_chunk_fwd
+ * (n_seqs = number of packed sequences when cu_seqlens is used, else B).
+ * The value does not depend on the contents of cu_seqlens.
+ */
+GDN_API size_t gdn_chunk_fwd_workspace_bytes(int B, int T, int H, int HV, int dk,
+                                     int dv, int chunk, int gate_mode,
+                                     int n_seqs, int dtype);
+
+/*
+ * Forward pass of the gated delta rule in chunk-parallel WY form.
+ *
+ * Layouts (contiguous, row-major; "dt" = dtype):
+ *   q, k   [B, T, H, dk]   dt          v, o   [B, T, HV, dv]   dt
+ *   g      [B, T, HV] (GDN) or [B, T, HV, dk] (KDA)          fp32, <= 0
+ *   beta   [B, T, HV]                                          fp32
+ *   h0, hT [N, HV, dk, dv]  fp32, K-first (N = B, or n_seqs when packed)
+ *   cu_seqlens  [n_seqs + 1] int32, device; packed sequences (then B == 1
+ *               and T is the total token count); NULL for plain batches.
+ *
+ * h0 may be NULL (zero initial state); hT may be NULL (final state not
+ * written).  hT must not overlap h0, and o must not overlap q, k, v, g or
+ * beta.  Every pointer must be 16-byte aligned.  scale multiplies the read
+ * (dk^-0.5 is usual).  chunk is the sub-chunk length C of the WY form.
+ *
+ * Supported domain: dk, dv in {64, 128}; chunk in {32, 64}; dtype F32 or BF16;
+ * HV a multiple of H.  Anything else valid returns GDN_ERR_UNSUPPORTED.
+ * Packed sequences of length 0 are allowed: their hT is h0 (or 0).
+ * T == 0 is allowed; q, k, v, g, beta and o may then be NULL.
+ *
+ * Workspace: at least gdn_chunk_fwd_workspace_bytes(...) bytes, 256-byte
+ * aligned, owned by the caller, not shared by two calls in flight.  Its first
+ * 256 bytes hold the device status word (GDN_FLAG_*), cleared by each call;
+ * read it back with gdn_read_device_flags.
+ *
+ * Numerics: fp32 state and accumulation; every product that touches the
+ * state, the solved tiles or the new values keeps at least 16 mantissa bits
+ * (operands split into two bf16 halves); o is rounded once, to dtype.
+ */
+GDN_API gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *g, const float *beta, const float *h0,
+                         void *o, float *hT, const int32_t *cu_seqlens,
+                         int n_seqs, int B, int T, int H, int HV, int dk,
+                         int dv, int chunk, float scale, int gate_mode,
+                         int dtype, void *workspace, size_t workspace_bytes,
+                         gdn_stream_t stream);
+
+/*
+ * The two halves of gdn_chunk_fwd, for callers that schedule them apart (to
+ * time each kernel, or to overlap one layer's prep with another's scan).
+ * Same arguments and checks as gdn_chunk_fwd.  gdn_chunk_fwd_prep clears the
+ * status word and runs the state-independent chunk-prep kernel, which writes
+ * the per-chunk tiles into `workspace` (it reads q, k, g, beta, cu_seqlens);
+ * gdn_chunk_fwd_scan runs the serial scan kernel, which reads those tiles and
+ * writes o and hT.  A scan must follow, in stream order, a prep with the same
+ * arguments and workspace; gdn_chunk_fwd_prep followed by gdn_chunk_fwd_scan
+ * computes exactly what gdn_chunk_fwd computes.
+ */
+GDN_API gdn_status gdn_chunk_fwd_prep(const void *q, const void *k, const void *v,
+                              const float *g, const float *beta, const float *h0,
+                              void *o, float *hT, const int32_t *cu_seqlens,
+                              int n_seqs, int B, int T, int H, int HV, int dk,
+                              int dv, int chunk, float scale, int gate_mode,
+                              int dtype, void *workspace, size_t workspace_bytes,
+                              gdn_stream_t stream);
+GDN_API gdn_status gdn_chunk_fwd_scan(const void *q, const void *k, const void *v,
+                              const float *g, const float *beta, const float *h0,
+                              void *o, float *hT, const int32_t *cu_seqlens,
+                              int n_seqs, int B, int T, int H, int HV, int dk,
+                              int dv, int chunk, float scale, int gate_mode,
+                              int dtype, void *workspace, size_t workspace_bytes,
+                              gdn_stream_t stream);
+
+/*
+ * Copy the device status word of `workspace` to *flags_out (host pointer)
+ * after all work queued on `stream` so far has finished (synchronises the
+ * stream).  Returns GDN_ERR_INVALID_ARG for NULL arguments and GDN_ERR_CUDA
+ * if the copy fails (including an earlier asynchronous fault).
+ */
+GDN_API gdn_status gdn_read_device_flags(const void *workspace, uint32_t *flags_out,
+                                 gdn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

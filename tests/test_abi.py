@@ -1,0 +1,120 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/gdn.h declares, and refuses malformed or unsupported requests before
+touching the device (explicit refusal of unsupported inputs, logismos issue
+#46 "Acceptance").  Fake device addresses are fine here: a refused call
+dereferences nothing."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from chunkwise_gated_delta_gdn_gb300 import build as cuda_build
+from chunkwise_gated_delta_gdn_gb300 import gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return gdn.load()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "gdn.h")) as f:
+        src = f.read()
+    return sorted(set(re.findall(r"GDN_API\s+[\w\s\*]*?\b(gdn_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_symbols() == sorted(gdn.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert gdn.gdn_version() >= 100
+
+
+def test_status_strings(lib):
+    assert gdn.gdn_status_string(0) == "GDN_OK"
+    assert gdn.gdn_status_string(2) == "GDN_ERR_UNSUPPORTED"
+    assert gdn.gdn_status_string(99) == "GDN_ERR_UNKNOWN"
+
+
+def test_workspace_query(lib):
+    ws = gdn.gdn_chunk_fwd_workspace_bytes(1, 32768, 16, 48, 128, 128, 64, 0, 1, 1)
+    # header + (T/C + N) slots x HV x (T and Aqk, C x C fp32)
+    assert ws == 256 + (32768 // 64 + 1) * 48 * 2 * 64 * 64 * 4
+    assert gdn.gdn_chunk_fwd_workspace_bytes(1, 100, 2, 4, 96, 128, 64, 0, 1, 1) == 0
+    assert gdn.gdn_chunk_fwd_workspace_bytes(1, 100, 3, 4, 128, 128, 64, 0, 1, 1) == 0
+
+
+# fake, 256-byte aligned, far-apart device addresses
+BASE = 1 << 40
+STRIDE = 1 << 34
+
+
+def addr(i):
+    return ctypes.c_void_p(BASE + i * STRIDE)
+
+
+def call(lib, **kw):
+    a = dict(q=addr(0), k=addr(1), v=addr(2), g=addr(3), beta=addr(4), h0=addr(5),
+             o=addr(6), hT=addr(7), cu=None, n_seqs=1, B=1, T=128, H=2, HV=4, dk=128,
+             dv=128, chunk=64, scale=0.088, gate_mode=0, dtype=1, ws=addr(8),
+             ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.gdn_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["o"],
+                             a["hT"], a["cu"], a["n_seqs"], a["B"], a["T"], a["H"],
+                             a["HV"], a["dk"], a["dv"], a["chunk"], a["scale"],
+                             a["gate_mode"], a["dtype"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(q=None), gdn.GDN_ERR_INVALID_ARG),
+    (dict(v=None, T=5), gdn.GDN_ERR_INVALID_ARG),
+    (dict(o=None), gdn.GDN_ERR_INVALID_ARG),
+    (dict(B=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(T=-1), gdn.GDN_ERR_INVALID_ARG),
+    (dict(H=3), gdn.GDN_ERR_INVALID_ARG),           # HV % H != 0
+    (dict(gate_mode=2), gdn.GDN_ERR_INVALID_ARG),
+    (dict(dtype=7), gdn.GDN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), gdn.GDN_ERR_INVALID_ARG),
+    (dict(dk=96), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dv=256), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(chunk=16), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(chunk=128), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(q=ctypes.c_void_p(BASE + 8)), gdn.GDN_ERR_INVALID_ARG),   # misaligned
+    (dict(ws=ctypes.c_void_p(BASE + 8 * STRIDE + 16)), gdn.GDN_ERR_INVALID_ARG),
+    (dict(ws=None), gdn.GDN_ERR_WORKSPACE),
+    (dict(ws_bytes=1000), gdn.GDN_ERR_WORKSPACE),
+    (dict(hT=addr(5)), gdn.GDN_ERR_INVALID_ARG),    # hT aliases h0
+    (dict(o=addr(2)), gdn.GDN_ERR_INVALID_ARG),     # o aliases v
+    (dict(ws=addr(0)), gdn.GDN_ERR_INVALID_ARG),    # workspace aliases q
+    (dict(cu=addr(9), B=2, n_seqs=2), gdn.GDN_ERR_INVALID_ARG),  # packed needs B == 1
+    (dict(cu=addr(9), n_seqs=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(B=2, n_seqs=3), gdn.GDN_ERR_INVALID_ARG),
+])
+def test_refusals(lib, kw, status):
+    assert call(lib, **kw) == status
+
+
+def test_read_flags_rejects_null(lib):
+    out = ctypes.c_uint32(0)
+    assert lib.gdn_read_device_flags(None, ctypes.byref(out), None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_read_device_flags(addr(8), None, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_binding_refuses_to_run_without_library(tmp_path):
+    """The product path fails loudly when the CUDA library is missing."""
+    with pytest.raises(RuntimeError, match="libgdn.so not found"):
+        saved = gdn._lib
+        gdn._lib = None
+        try:
+            gdn.load(str(tmp_path / "missing.so"))
+        finally:
+            gdn._lib = saved
