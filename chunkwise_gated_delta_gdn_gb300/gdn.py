@@ -36,7 +36,7 @@ GDN_FLAG_BAD_SEQLENS = 1 << 2
 # every symbol include/gdn.h declares
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_chunk_fwd_workspace_bytes",
             "gdn_chunk_fwd", "gdn_chunk_fwd_prep", "gdn_chunk_fwd_scan",
-            "gdn_read_device_flags")
+            "gdn_chunk_fwd_noalloc", "gdn_read_device_flags")
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +76,10 @@ def load(path: Optional[str] = None):
             fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                            i32, i32, i32, i32, i32, f32, i32, i32, vp, sz, vp]
             fn.restype = i32
+        lib.gdn_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                              i32, i32, i32, i32, i32, i32, f32, i32, i32,
+                                              vp]
+        lib.gdn_chunk_fwd_noalloc.restype = i32
         lib.gdn_read_device_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gdn_read_device_flags.restype = i32
         _lib = lib

@@ -166,6 +166,33 @@ GDN_API gdn_status gdn_chunk_fwd_scan(const void *q, const void *k, const void *
                               gdn_stream_t stream);
 
 /*
+ * gdn_chunk_fwd for callers that cannot allocate device memory: a component
+ * inside a host framework that owns all device memory and gives it no
+ * allocation of its own, or a latency-critical loop that must not stall on
+ * an allocation.  (The pages describe no such entry point; it has no
+ * counterpart there.)
+ *
+ * Same arguments, layouts, checks and results as gdn_chunk_fwd, minus the
+ * workspace: the library uses a fixed 64 MiB device array of its own instead,
+ * reserved on every GPU that loads the library until the process exits.  The
+ * caller still provides q, k, v, g, beta, h0, o and hT.  Returns
+ * GDN_ERR_WORKSPACE when the request needs more than 64 MiB of workspace
+ * (gdn_chunk_fwd_workspace_bytes tells), GDN_ERR_CUDA when the array's
+ * device address cannot be obtained.  The first call on each device looks
+ * that address up (with the device current); make that first call before any
+ * stream capture.  All calls on a device share the one array: calls that
+ * overlap on the GPU race and must be serialised by the caller.  The device
+ * status word of these calls lives in that array and is not exposed.
+ */
+GDN_API gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                 const float *g, const float *beta,
+                                 const float *h0, void *o, float *hT,
+                                 const int32_t *cu_seqlens, int n_seqs, int B,
+                                 int T, int H, int HV, int dk, int dv, int chunk,
+                                 float scale, int gate_mode, int dtype,
+                                 gdn_stream_t stream);
+
+/*
  * Copy the device status word of `workspace` to *flags_out (host pointer)
  * after all work queued on `stream` so far has finished (synchronises the
  * stream).  Returns GDN_ERR_INVALID_ARG for NULL arguments and GDN_ERR_CUDA
