@@ -6,11 +6,58 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <cstddef>
+#include <cstring>
+#include <mutex>
 
 #include "gdn.h"
 #include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor [d2][d1][d0] (d0 contiguous), box {b0, 1, b2}, 128-byte swizzle
+bool map3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
+           uint32_t b2) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint32_t box[3] = {b0, 1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool make_scan_maps(ScanMaps &m, const void *q, const void *k, const void *v, int Ttot, int H,
+                    int HV, int dk, int dv, int chunk) {
+  std::memset(&m, 0, sizeof(m));
+  if (Ttot <= 0) return true;  // nothing will be loaded
+  if (!encode_fn()) return false;
+  return map3d(&m.q, q, dk, H, Ttot, 64, chunk) && map3d(&m.k, k, dk, H, Ttot, 64, chunk) &&
+         map3d(&m.v, v, dv, HV, Ttot, kScanTcSlice, chunk);
+}
+
+}  // namespace gdn
 
 namespace {
 
@@ -52,7 +99,11 @@ gdn_status plan(int B, int T, int H, int HV, int dk, int dv, int chunk,
   if (p.Ttot > INT32_MAX - 2L * chunk) return GDN_ERR_UNSUPPORTED;
   p.n_slots = p.Ttot / chunk + p.n_states;
   if (p.n_slots > INT32_MAX) return GDN_ERR_UNSUPPORTED;
-  p.tile_bytes = (size_t)p.n_slots * (size_t)HV * 2u * (size_t)chunk * (size_t)chunk * sizeof(float);
+  // fp32 inputs: T and Aqk as fp32 C x C tiles; bf16 inputs: one fp16 operand
+  // image per (chunk, value head)
+  const size_t per = dtype == GDN_BF16 ? (size_t)gdn::kPrepImageBytes
+                                       : 2u * (size_t)chunk * (size_t)chunk * sizeof(float);
+  p.tile_bytes = (size_t)p.n_slots * (size_t)HV * per;
   p.ws_bytes = gdn::kWorkspaceHeader + p.tile_bytes;
   return GDN_OK;
 }
@@ -145,15 +196,23 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
       pa.q = q; pa.k = k; pa.g = g; pa.beta = beta;
       pa.seq = seq; pa.H = H; pa.HV = HV; pa.scale = scale;
       pa.tiles = tiles; pa.flags = flags; pa.n_slots = (int)p.n_slots;
-      if (gdn::launch_prep(pa, chunk, dk, dtype, gate_mode, stream) != cudaSuccess) return GDN_ERR_CUDA;
+      const cudaError_t e = dtype == GDN_BF16 ? gdn::launch_prep_tc(pa, chunk, dk, gate_mode, stream)
+                                              : gdn::launch_prep(pa, chunk, dk, dtype, gate_mode, stream);
+      if (e != cudaSuccess) return GDN_ERR_CUDA;
     }
   }
+  gdn::ScanMaps maps;
+  if ((stages & kScan) && dtype == GDN_BF16 &&
+      !gdn::make_scan_maps(maps, q, k, v, (int)p.Ttot, H, HV, dk, dv, chunk))
+    return GDN_ERR_CUDA;
   if (stages & kScan) {
     gdn::ScanArgs sa;
     sa.q = q; sa.k = k; sa.v = v; sa.g = g; sa.beta = beta; sa.h0 = h0;
     sa.o = o; sa.hT = hT; sa.seq = seq; sa.H = H; sa.HV = HV; sa.dv = dv;
     sa.scale = scale; sa.tiles = tiles; sa.flags = flags;
-    if (gdn::launch_scan(sa, chunk, dk, dtype, gate_mode, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    const cudaError_t e = dtype == GDN_BF16 ? gdn::launch_scan_tc(sa, maps, chunk, dk, gate_mode, stream)
+                                            : gdn::launch_scan(sa, chunk, dk, dtype, gate_mode, stream);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
   }
   return GDN_OK;
 }

@@ -2,6 +2,7 @@
 // kernel translation units (gdn_prep.cu, gdn_scan.cu).  Not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -9,8 +10,14 @@ namespace gdn {
 
 // Bytes at the start of the workspace reserved for the device status word.
 constexpr size_t kWorkspaceHeader = 256;
-// Width of one dv slice handled by a scan CTA.
+// Width of one dv slice handled by a scan CTA (fp32 path / bf16 path).
 constexpr int kScanSlice = 32;
+constexpr int kScanTcSlice = 64;
+// The bf16 path's per-(chunk, value head) operand image written by the prep
+// kernel: 192 rows x 64 fp16, K-major with the 128-byte swizzle
+// (rows 0..127 = P1 = Kt^T T, rows 128..191 = Aqk T).
+constexpr int kPrepImageRows = 192;
+constexpr int kPrepImageBytes = kPrepImageRows * 128;
 
 // Where packed sequence n starts: cu_seqlens[n], or n*T for plain batches.
 // Sequence n owns the chunk slots [floor(start_n / C) + n, ...): one slot per
@@ -49,6 +56,7 @@ struct ScanArgs {
 constexpr uint32_t kFlagPositiveGate = 1u << 0;
 constexpr uint32_t kFlagNonfinite = 1u << 1;
 constexpr uint32_t kFlagBadSeqlens = 1u << 2;
+constexpr uint32_t kFlagTimeout = 1u << 3;
 
 // Launchers; return cudaErrorInvalidValue for an uncompiled combination.
 // dtype: 0 = fp32, 1 = bf16.  gate: 0 = scalar (GDN), 1 = per key (KDA).
@@ -56,5 +64,19 @@ cudaError_t launch_prep(const PrepArgs &a, int chunk, int dk, int dtype,
                         int gate, cudaStream_t stream);
 cudaError_t launch_scan(const ScanArgs &a, int chunk, int dk, int dtype,
                         int gate, cudaStream_t stream);
+// TMA descriptors of the bf16 path's scan: q, k as [Ttot][H][dk] and v as
+// [Ttot][HV][dv], boxes of 64 columns x 1 head x C tokens, 128-byte swizzle.
+struct ScanMaps {
+  CUtensorMap q, k, v;
+};
+// Encode the three maps (host); false when the driver refuses.
+bool make_scan_maps(ScanMaps &m, const void *q, const void *k, const void *v, int Ttot,
+                    int H, int HV, int dk, int dv, int chunk);
+
+// bf16 path: prep writing fp16 operand images, tcgen05 scan consuming them
+cudaError_t launch_prep_tc(const PrepArgs &a, int chunk, int dk, int gate,
+                           cudaStream_t stream);
+cudaError_t launch_scan_tc(const ScanArgs &a, const ScanMaps &maps, int chunk, int dk,
+                           int gate, cudaStream_t stream);
 
 }  // namespace gdn

@@ -1,0 +1,361 @@
+// gdn_prep_tc.cu -- the state-independent chunk-prep kernel of the bf16 path.
+//
+// One CTA (128 threads) per (chunk slot, value head).  From the chunk's keys,
+// queries, gates and beta it forms, in fp32:
+//   b      cumulative natural-log gates (per key channel for KDA)
+//   A      = strict-lower(beta_r sum_c k_rc k_sc exp(b_rc - b_sc))
+//   Aqk    = lower-incl-diag(scale sum_c q_rc k_sc exp(b_rc - b_sc))
+//   T      = (I + A)^-1   (blocked: 16 x 16 diagonal blocks by forward
+//            substitution, then block rows by products against the solved
+//            blocks; ROCm/rocm-libraries PR #11223, "Levers" 3)
+//   P1     = Kt^T T       (Kt_s = k_s exp(b_last - b_s); dk x C)
+//   AqkT   = Aqk T        (C x C)
+// and writes P1 and AqkT, rounded once to fp16, as one 24 KB operand image in
+// the scan kernel's shared-memory layout (K-major, 128-byte swizzle, 192 rows
+// of 64 elements: rows 0..127 = P1 (rows >= dk zero), rows 128..191 = AqkT,
+// columns >= C zero).  With Y = diag(beta)(V - Kg S) the scan then needs only
+//   S <- diag(exp(b_last)) S + P1 Y     and     O = Qg S + AqkT Y,
+// the WY products W = T diag(beta) Kg and U = T diag(beta) V of stratat pull
+// #1296 ("What this is") folded into P1 and AqkT so that no dk-wide W ever
+// crosses HBM.  Every product here runs on the tensor cores in split bf16
+// (16-bit mantissa operands, fp32 accumulation); the images are the only
+// rounding to fp16.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "gdn_device.cuh"
+#include "gdn_internal.h"
+#include "gdn_sm100.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 128;
+
+template <int C, int DK, int GATE>
+struct PrepTcSmem {
+  static constexpr int LDB = DK + 8;  // bf16 row stride of K / Q
+  static constexpr int LDC = C + 4;   // fp32 row stride of C x C tiles
+  static constexpr int LDG = GATE == 0 ? 1 : DK + 4;
+  // byte offsets
+  static constexpr int kK = 0;
+  static constexpr int kQ = kK + C * LDB * 2;  // Q, then (with A) the image
+  static constexpr int QSZ = (C * LDB * 2 + C * LDC * 4 >= kPrepImageBytes)
+                                 ? C * LDB * 2
+                                 : kPrepImageBytes - C * LDC * 4;
+  static constexpr int kA = kQ + QSZ;
+  static constexpr int kImgSpan = QSZ + C * LDC * 4;  // Q + A regions
+  static constexpr int kAqk = kA + C * LDC * 4;
+  static constexpr int kT = kAqk + C * LDC * 4;
+  static constexpr int kR = kT + C * LDC * 4;                  // 16 x LDC scratch
+  static constexpr int kG = kR + 16 * LDC * 4;                 // gates -> b -> Kt (KDA)
+  static constexpr int kBeta = kG + C * LDG * 4;
+  static constexpr int kMeta = kBeta + C * 4;
+  static constexpr int kBytes = kMeta + 16;
+  static_assert(kImgSpan >= kPrepImageBytes, "image must fit the Q + A regions");
+};
+
+// acc[nt] += A * B over KDIM for a 16 x 8*NT tile; A row-major bf16 (exact),
+// B given as B^T row-major bf16 (i.e. B[k][n] = Bt[n][k]), both in shared memory
+template <int KDIM, int NT>
+__device__ __forceinline__ void mma_bf16_exact(float (&acc)[NT][4], const __nv_bfloat16 *A,
+                                               int lda, const __nv_bfloat16 *Bt, int ldb) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+#pragma unroll 4
+  for (int k0 = 0; k0 < KDIM; k0 += 16) {
+    uint32_t a[4];
+    a[0] = *reinterpret_cast<const uint32_t *>(A + gq * lda + k0 + 2 * tq);
+    a[1] = *reinterpret_cast<const uint32_t *>(A + (gq + 8) * lda + k0 + 2 * tq);
+    a[2] = *reinterpret_cast<const uint32_t *>(A + gq * lda + k0 + 2 * tq + 8);
+    a[3] = *reinterpret_cast<const uint32_t *>(A + (gq + 8) * lda + k0 + 2 * tq + 8);
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+      const __nv_bfloat16 *b = Bt + (nt * 8 + gq) * ldb + k0 + 2 * tq;
+      mma16816(acc[nt], a, *reinterpret_cast<const uint32_t *>(b),
+               *reinterpret_cast<const uint32_t *>(b + 8));
+    }
+  }
+}
+
+__device__ __forceinline__ void put_f16(unsigned char *img, int row, int col, float v) {
+  *reinterpret_cast<__half *>(img + sm100::kmajor_off(row, col, kPrepImageRows)) = __float2half_rn(v);
+}
+
+template <int C, int DK, int GATE>
+__global__ void __launch_bounds__(kThreads)
+gdn_prep_tc_kernel(const PrepArgs a) {
+  using SM = PrepTcSmem<C, DK, GATE>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __nv_bfloat16 *Kb = reinterpret_cast<__nv_bfloat16 *>(smem + SM::kK);
+  __nv_bfloat16 *Qb = reinterpret_cast<__nv_bfloat16 *>(smem + SM::kQ);
+  float *As = reinterpret_cast<float *>(smem + SM::kA);
+  float *Aqks = reinterpret_cast<float *>(smem + SM::kAqk);
+  float *Ts = reinterpret_cast<float *>(smem + SM::kT);
+  float *Rs = reinterpret_cast<float *>(smem + SM::kR);
+  float *Gs = reinterpret_cast<float *>(smem + SM::kG);
+  float *Bs = reinterpret_cast<float *>(smem + SM::kBeta);
+  int *meta = reinterpret_cast<int *>(smem + SM::kMeta);
+  unsigned char *img = smem + SM::kQ;  // valid once Q and A are dead
+
+  const int slot = blockIdx.x, hv = blockIdx.y;
+  const int hq = hv / (a.HV / a.H);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int LDB = SM::LDB, LDC = SM::LDC, LDG = SM::LDG;
+
+  // ---- slot -> (sequence, chunk) ----
+  if (tid == 0) {
+    int lo = 0, hi = a.seq.n_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (slot_base<C>(a.seq, mid) <= slot) lo = mid; else hi = mid - 1;
+    }
+    int start, end;
+    int valid = seq_ok(a.seq, lo, start, end) ? 1 : 0;
+    const long c = (long)slot - slot_base<C>(a.seq, lo);
+    const long t0 = (long)start + c * C;
+    if (c < 0 || t0 >= end) valid = 0;
+    meta[0] = valid ? (int)t0 : 0;
+    meta[1] = valid ? (int)min((long)C, (long)end - t0) : 0;
+    meta[2] = valid;
+  }
+  __syncthreads();
+  if (!meta[2]) return;
+  const int t0 = meta[0], L = meta[1];
+
+  // ---- loads ----
+  {
+    const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(a.k) + ((long)t0 * a.H + hq) * DK;
+    const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(a.q) + ((long)t0 * a.H + hq) * DK;
+    constexpr int PER = DK / 8;
+    for (int idx = tid; idx < C * PER; idx += kThreads) {
+      const int r = idx / PER, c8 = (idx % PER) * 8;
+      uint4 kv = make_uint4(0, 0, 0, 0), qv = make_uint4(0, 0, 0, 0);
+      if (r < L) {
+        kv = __ldg(reinterpret_cast<const uint4 *>(kg + (long)r * a.H * DK + c8));
+        qv = __ldg(reinterpret_cast<const uint4 *>(qg + (long)r * a.H * DK + c8));
+      }
+      *reinterpret_cast<uint4 *>(Kb + r * LDB + c8) = kv;
+      *reinterpret_cast<uint4 *>(Qb + r * LDB + c8) = qv;
+    }
+  }
+  bool positive = false;
+  if constexpr (GATE == 0) {
+    for (int r = tid; r < C; r += kThreads) {
+      const float gv = r < L ? __ldg(a.g + (long)(t0 + r) * a.HV + hv) : 0.f;
+      positive |= gv > 0.f;
+      Gs[r] = gv;
+    }
+  } else {
+    for (int idx = tid; idx < C * DK / 4; idx += kThreads) {
+      const int r = idx / (DK / 4), c4 = (idx % (DK / 4)) * 4;
+      float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < L) gv = __ldg(reinterpret_cast<const float4 *>(a.g + ((long)(t0 + r) * a.HV + hv) * DK + c4));
+      positive |= (gv.x > 0.f) | (gv.y > 0.f) | (gv.z > 0.f) | (gv.w > 0.f);
+      *reinterpret_cast<float4 *>(Gs + r * LDG + c4) = gv;
+    }
+  }
+  for (int r = tid; r < C; r += kThreads)
+    Bs[r] = r < L ? __ldg(a.beta + (long)(t0 + r) * a.HV + hv) : 0.f;
+  for (int idx = tid; idx < C * LDC; idx += kThreads) Ts[idx] = 0.f;
+  if (__syncthreads_or(positive) && tid == 0) atomicOr(a.flags, kFlagPositiveGate);
+
+  // ---- cumulative log-gates ----
+  if constexpr (GATE == 0) {
+    if (warp == 0) {
+      float x0 = lane < C ? Gs[lane] : 0.f;
+      float x1 = lane + 32 < C ? Gs[lane + 32] : 0.f;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const float y0 = __shfl_up_sync(0xffffffffu, x0, d);
+        const float y1 = __shfl_up_sync(0xffffffffu, x1, d);
+        if (lane >= d) { x0 += y0; x1 += y1; }
+      }
+      x1 += __shfl_sync(0xffffffffu, x0, 31);
+      if (lane < C) Gs[lane] = x0;
+      if (lane + 32 < C) Gs[lane + 32] = x1;
+    }
+  } else {
+    for (int c = tid; c < DK; c += kThreads) {
+      float run = 0.f;
+      for (int r = 0; r < C; r++) {
+        run += Gs[r * LDG + c];
+        Gs[r * LDG + c] = run;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- A and Aqk ----
+  if constexpr (GATE == 0) {
+    // tasks: {K K^T, Q K^T} x row tiles of 16; all C columns (NT = C/8)
+    constexpr int NMT = C / 16, NT = C / 8;
+    for (int task = warp; task < 2 * NMT; task += kThreads / 32) {
+      const int which = task / NMT, m0 = (task % NMT) * 16;
+      float acc[NT][4] = {};
+      mma_bf16_exact<DK, NT>(acc, (which == 0 ? Kb : Qb) + m0 * LDB, LDB, Kb, LDB);
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const int r = m0 + acc_row(e), s = acc_col(nt, e);
+          float v = 0.f;
+          if (which == 0) {
+            if (s < r) v = Bs[r] * acc[nt][e] * __expf(Gs[r] - Gs[s]);
+            As[r * LDC + s] = v;
+          } else {
+            if (s <= r) v = a.scale * acc[nt][e] * __expf(Gs[r] - Gs[s]);
+            Aqks[r * LDC + s] = v;
+          }
+        }
+    }
+  } else {
+    constexpr int NPAIR = C * (C + 1) / 2;
+    for (int p = warp; p < NPAIR; p += kThreads / 32) {
+      int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
+      while ((r + 1) * (r + 2) / 2 <= p) r++;
+      while (r * (r + 1) / 2 > p) r--;
+      const int s = p - r * (r + 1) / 2;
+      float kk = 0.f, qk = 0.f;
+      for (int c = lane; c < DK; c += 32) {
+        const float d = __expf(Gs[r * LDG + c] - Gs[s * LDG + c]);
+        const float ks = __bfloat162float(Kb[s * LDB + c]) * d;
+        kk += __bfloat162float(Kb[r * LDB + c]) * ks;
+        qk += __bfloat162float(Qb[r * LDB + c]) * ks;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        kk += __shfl_xor_sync(0xffffffffu, kk, off);
+        qk += __shfl_xor_sync(0xffffffffu, qk, off);
+      }
+      if (lane == 0) {
+        As[r * LDC + s] = s < r ? Bs[r] * kk : 0.f;
+        Aqks[r * LDC + s] = a.scale * qk;
+      }
+    }
+    for (int idx = tid; idx < C * C; idx += kThreads) {
+      const int r = idx / C, s = idx % C;
+      if (s > r) { As[r * LDC + s] = 0.f; Aqks[r * LDC + s] = 0.f; }
+    }
+  }
+  __syncthreads();
+
+  // ---- T = (I + A)^-1 ----
+  constexpr int NB = C / 16;
+  if (tid < NB * 16) {
+    // diagonal block I, column j: right-looking substitution
+    const int I = tid / 16, j = tid % 16, o = 16 * I;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; r++) x[r] = (r == j) ? 1.f : 0.f;
+#pragma unroll
+    for (int s = 0; s < 16; s++) {
+      const float xs = x[s];
+#pragma unroll
+      for (int r = s + 1; r < 16; r++) x[r] -= As[(o + r) * LDC + o + s] * xs;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; r++) Ts[(o + r) * LDC + o + j] = x[r];
+  }
+  __syncthreads();
+  // block row I:  R = A[I, 0:I] T[0:I, 0:I],  T[I, 0:I] = -T_II R
+  for (int I = 1; I < NB; I++) {
+    const int w = 16 * I;  // width of the solved part
+    for (int idx = tid; idx < 16 * w; idx += kThreads) {
+      const int m = idx / w, j = idx % w;
+      float acc = 0.f;
+      for (int s = (j & ~15); s < w; s++) acc += As[(w + m) * LDC + s] * Ts[s * LDC + j];
+      Rs[m * LDC + j] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < 16 * w; idx += kThreads) {
+      const int m = idx / w, j = idx % w;
+      float acc = 0.f;
+      for (int p = 0; p <= m; p++) acc += Ts[(w + m) * LDC + w + p] * Rs[p * LDC + j];
+      Ts[(w + m) * LDC + j] = -acc;
+    }
+    __syncthreads();
+  }
+
+  // ---- KDA: Kt = k * exp(b_last - b) in place of the cumulative gates ----
+  if constexpr (GATE == 1) {
+    for (int c = tid; c < DK; c += kThreads) {
+      const float bl = Gs[(C - 1) * LDG + c];
+      for (int r = 0; r < C; r++)
+        Gs[r * LDG + c] = __bfloat162float(Kb[r * LDB + c]) * __expf(bl - Gs[r * LDG + c]);
+    }
+  }
+  // ---- the image (Q and A are dead now): zero, then P1 and AqkT ----
+  for (int idx = tid; idx < kPrepImageBytes / 16; idx += kThreads)
+    reinterpret_cast<uint4 *>(img)[idx] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+
+  // AqkT = Aqk T  (3-pass split)
+  {
+    constexpr int NMT = C / 16, NNG = C / 32;
+    for (int task = warp; task < NMT * NNG; task += kThreads / 32) {
+      const int m0 = (task / NNG) * 16, n0 = (task % NNG) * 32;
+      float acc[4][4] = {};
+      warp_mma<C, 4, false, false>(
+          acc, [&](int m, int k) { return Aqks[(m0 + m) * LDC + k]; },
+          [&](int k, int n) { return Ts[k * LDC + n0 + n]; });
+#pragma unroll
+      for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++)
+          put_f16(img, kPrepImageRows - 64 + m0 + acc_row(e), n0 + acc_col(nt, e), acc[nt][e]);
+    }
+  }
+  // P1 = Kt^T T  (GDN: K exact, row-scaled T split; KDA: Kt split)
+  {
+    const float blast = GATE == 0 ? Gs[C - 1] : 0.f;
+    constexpr int NMT = DK / 16, NNG = C / 32;
+    for (int task = warp; task < NMT * NNG; task += kThreads / 32) {
+      const int m0 = (task / NNG) * 16, n0 = (task % NNG) * 32;
+      float acc[4][4] = {};
+      if constexpr (GATE == 0) {
+        warp_mma<C, 4, true, false>(
+            acc, [&](int m, int k) { return __bfloat162float(Kb[k * LDB + m0 + m]); },
+            [&](int k, int n) { return __expf(blast - Gs[k]) * Ts[k * LDC + n0 + n]; });
+      } else {
+        warp_mma<C, 4, false, false>(
+            acc, [&](int m, int k) { return Gs[k * LDG + m0 + m]; },
+            [&](int k, int n) { return Ts[k * LDC + n0 + n]; });
+      }
+#pragma unroll
+      for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) put_f16(img, m0 + acc_row(e), n0 + acc_col(nt, e), acc[nt][e]);
+    }
+  }
+  __syncthreads();
+
+  // ---- image -> workspace ----
+  uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(a.tiles) +
+                                         ((size_t)slot * a.HV + hv) * kPrepImageBytes);
+  for (int idx = tid; idx < kPrepImageBytes / 16; idx += kThreads)
+    dst[idx] = reinterpret_cast<const uint4 *>(img)[idx];
+}
+
+template <int C, int DK, int GATE>
+cudaError_t launch_one(const PrepArgs &a, cudaStream_t stream) {
+  using SM = PrepTcSmem<C, DK, GATE>;
+  auto kern = gdn_prep_tc_kernel<C, DK, GATE>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+  if (err != cudaSuccess) return err;
+  kern<<<dim3(a.n_slots, a.HV), kThreads, SM::kBytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prep_tc(const PrepArgs &a, int chunk, int dk, int gate, cudaStream_t stream) {
+  if (chunk == 64 && dk == 128) return gate ? launch_one<64, 128, 1>(a, stream) : launch_one<64, 128, 0>(a, stream);
+  if (chunk == 64 && dk == 64) return gate ? launch_one<64, 64, 1>(a, stream) : launch_one<64, 64, 0>(a, stream);
+  if (chunk == 32 && dk == 128) return gate ? launch_one<32, 128, 1>(a, stream) : launch_one<32, 128, 0>(a, stream);
+  if (chunk == 32 && dk == 64) return gate ? launch_one<32, 64, 1>(a, stream) : launch_one<32, 64, 0>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gdn

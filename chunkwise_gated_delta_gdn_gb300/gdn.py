@@ -32,6 +32,7 @@ GDN_BF16 = 1
 GDN_FLAG_POSITIVE_GATE = 1 << 0
 GDN_FLAG_NONFINITE = 1 << 1
 GDN_FLAG_BAD_SEQLENS = 1 << 2
+GDN_FLAG_TIMEOUT = 1 << 3
 
 # every symbol include/gdn.h declares
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_chunk_fwd_workspace_bytes",

@@ -81,8 +81,10 @@ typedef enum gdn_dtype {
 enum {
   GDN_FLAG_POSITIVE_GATE = 1u << 0, /* some log-gate g > 0 (a decay above 1) */
   GDN_FLAG_NONFINITE = 1u << 1,     /* a non-finite value was written to o/hT */
-  GDN_FLAG_BAD_SEQLENS = 1u << 2    /* cu_seqlens not 0 = c0 <= c1 <= .. = T;
+  GDN_FLAG_BAD_SEQLENS = 1u << 2,   /* cu_seqlens not 0 = c0 <= c1 <= .. = T;
                                        affected sequences were skipped */
+  GDN_FLAG_TIMEOUT = 1u << 3        /* an internal wait ran out of its time
+                                       budget; the results are not valid */
 };
 
 /* Library version, major*10000 + minor*100 + patch. */
@@ -127,9 +129,12 @@ GDN_API size_t gdn_chunk_fwd_workspace_bytes(int B, int T, int H, int HV, int dk
  * 256 bytes hold the device status word (GDN_FLAG_*), cleared by each call;
  * read it back with gdn_read_device_flags.
  *
- * Numerics: fp32 state and accumulation; every product that touches the
- * state, the solved tiles or the new values keeps at least 16 mantissa bits
- * (operands split into two bf16 halves); o is rounded once, to dtype.
+ * Numerics: fp32 state, fp32 accumulation, o rounded once to dtype.  fp32
+ * inputs: every product keeps at least 16 mantissa bits (operands split into
+ * two bf16 halves).  bf16 inputs: tensor-core operands are fp16 (11 mantissa
+ * bits; key, query, state and per-chunk tiles must stay below 65504 in
+ * magnitude, which unit-norm keys/queries and decays <= 1 guarantee), and the
+ * per-chunk solve runs in fp32.
  */
 GDN_API gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *g, const float *beta, const float *h0,

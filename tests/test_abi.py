@@ -46,8 +46,11 @@ def test_status_strings(lib):
 
 
 def test_workspace_query(lib):
-    ws = gdn.gdn_chunk_fwd_workspace_bytes(1, 32768, 16, 48, 128, 128, 64, 0, 1, 1)
-    # header + (T/C + N) slots x HV x (T and Aqk, C x C fp32)
+    # bf16: header + (T/C + N) slots x HV x one 24 KB fp16 operand image
+    ws = gdn.gdn_chunk_fwd_workspace_bytes(1, 32768, 16, 48, 128, 128, 64, 0, 1, gdn.GDN_BF16)
+    assert ws == 256 + (32768 // 64 + 1) * 48 * 192 * 128
+    # fp32: header + slots x HV x (T and Aqk, C x C fp32)
+    ws = gdn.gdn_chunk_fwd_workspace_bytes(1, 32768, 16, 48, 128, 128, 64, 0, 1, gdn.GDN_F32)
     assert ws == 256 + (32768 // 64 + 1) * 48 * 2 * 64 * 64 * 4
     assert gdn.gdn_chunk_fwd_workspace_bytes(1, 100, 2, 4, 96, 128, 64, 0, 1, 1) == 0
     assert gdn.gdn_chunk_fwd_workspace_bytes(1, 100, 3, 4, 128, 128, 64, 0, 1, 1) == 0
