@@ -189,6 +189,10 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
   seq.Ttot = (int)p.Ttot;
   float *tiles = reinterpret_cast<float *>(static_cast<char *>(workspace) + gdn::kWorkspaceHeader);
 
+  gdn::ScanMaps maps;
+  if (dtype == GDN_BF16 &&
+      !gdn::make_scan_maps(maps, q, k, v, (int)p.Ttot, H, HV, dk, dv, chunk))
+    return GDN_ERR_CUDA;
   if (stages & kPrep) {
     if (cudaMemsetAsync(flags, 0, sizeof(uint32_t), stream) != cudaSuccess) return GDN_ERR_CUDA;
     if (p.Ttot > 0) {
@@ -196,15 +200,16 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
       pa.q = q; pa.k = k; pa.g = g; pa.beta = beta;
       pa.seq = seq; pa.H = H; pa.HV = HV; pa.scale = scale;
       pa.tiles = tiles; pa.flags = flags; pa.n_slots = (int)p.n_slots;
-      const cudaError_t e = dtype == GDN_BF16 ? gdn::launch_prep_tc(pa, chunk, dk, gate_mode, stream)
-                                              : gdn::launch_prep(pa, chunk, dk, dtype, gate_mode, stream);
+      cudaError_t e;
+      if (dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR)
+        e = gdn::launch_prep_tmem(pa, maps, chunk, dk, stream);
+      else if (dtype == GDN_BF16)
+        e = gdn::launch_prep_tc(pa, chunk, dk, gate_mode, stream);
+      else
+        e = gdn::launch_prep(pa, chunk, dk, dtype, gate_mode, stream);
       if (e != cudaSuccess) return GDN_ERR_CUDA;
     }
   }
-  gdn::ScanMaps maps;
-  if ((stages & kScan) && dtype == GDN_BF16 &&
-      !gdn::make_scan_maps(maps, q, k, v, (int)p.Ttot, H, HV, dk, dv, chunk))
-    return GDN_ERR_CUDA;
   if (stages & kScan) {
     gdn::ScanArgs sa;
     sa.q = q; sa.k = k; sa.v = v; sa.g = g; sa.beta = beta; sa.h0 = h0;

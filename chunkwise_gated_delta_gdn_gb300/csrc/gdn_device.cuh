@@ -140,6 +140,31 @@ __device__ __forceinline__ void warp_mma(float (&acc)[NT][4], FA a_at, FB b_at) 
   }
 }
 
+// As warp_mma, with the contraction length `kdim` (a multiple of 16) known
+// only at run time.
+template <int NT, bool AX, bool BX, typename FA, typename FB>
+__device__ __forceinline__ void warp_mma_rt(float (&acc)[NT][4], int kdim, FA a_at, FB b_at) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+#pragma unroll 1
+  for (int k0 = 0; k0 < kdim; k0 += 16) {
+    uint32_t ahi[4], alo[4];
+    split2(a_at(gq, k0 + 2 * tq), a_at(gq, k0 + 2 * tq + 1), ahi[0], alo[0]);
+    split2(a_at(gq + 8, k0 + 2 * tq), a_at(gq + 8, k0 + 2 * tq + 1), ahi[1], alo[1]);
+    split2(a_at(gq, k0 + 2 * tq + 8), a_at(gq, k0 + 2 * tq + 9), ahi[2], alo[2]);
+    split2(a_at(gq + 8, k0 + 2 * tq + 8), a_at(gq + 8, k0 + 2 * tq + 9), ahi[3], alo[3]);
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+      const int n = nt * 8 + gq;
+      uint32_t bhi0, blo0, bhi1, blo1;
+      split2(b_at(k0 + 2 * tq, n), b_at(k0 + 2 * tq + 1, n), bhi0, blo0);
+      split2(b_at(k0 + 2 * tq + 8, n), b_at(k0 + 2 * tq + 9, n), bhi1, blo1);
+      if constexpr (!AX) mma16816(acc[nt], alo, bhi0, bhi1);
+      if constexpr (!BX) mma16816(acc[nt], ahi, blo0, blo1);
+      mma16816(acc[nt], ahi, bhi0, bhi1);
+    }
+  }
+}
+
 // Row / column of accumulator element e of n-tile nt for this lane.
 __device__ __forceinline__ int acc_row(int e) { return ((threadIdx.x & 31) >> 2) + ((e & 2) ? 8 : 0); }
 __device__ __forceinline__ int acc_col(int nt, int e) { return nt * 8 + 2 * (threadIdx.x & 3) + (e & 1); }

@@ -78,5 +78,8 @@ cudaError_t launch_prep_tc(const PrepArgs &a, int chunk, int dk, int gate,
                            cudaStream_t stream);
 cudaError_t launch_scan_tc(const ScanArgs &a, const ScanMaps &maps, int chunk, int dk,
                            int gate, cudaStream_t stream);
+// bf16 scalar-gate prep on tensor memory (same image as launch_prep_tc)
+cudaError_t launch_prep_tmem(const PrepArgs &a, const ScanMaps &maps, int chunk, int dk,
+                             cudaStream_t stream);
 
 }  // namespace gdn

@@ -163,11 +163,45 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     const uint32_t sS = smem_addr(sm + SM::kS), sY = smem_addr(sm + SM::kY);
     bool nonfinite = false;
     float o_part[NS];
+    const bool key_warp = warp * 32 < C;
+    const bool query_warp = warp >= 2 && (warp - 2) * 32 < C;
+
+    // all NS columns of this thread's lane at column `col` (one wait)
+    auto lane_row = [&](uint32_t col, float (&v)[NS]) {
+      uint32_t r0[32], r1[32];
+      tmem_ld32_nowait(col + lane_base, r0);
+      tmem_ld32_nowait(col + lane_base + 32, r1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; i++) { v[i] = __uint_as_float(r0[i]); v[32 + i] = __uint_as_float(r1[i]); }
+    };
+    // O of chunk cc = partial (Qg S) + AqkT Y, rounded to bf16 and stored
+    auto output_rows = [&](int cc) {
+      const int r = t - 64;
+      const int t0 = start + cc * C;
+      const int L = min(C, end - t0);
+      float d[NS];
+      lane_row(tD3, d);
+      if (r < L) {
+        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((long)(t0 + r) * a.HV + hv) * a.dv + col0;
+#pragma unroll
+        for (int ch = 0; ch < NS / 8; ch++) {
+          uint4 pk;
+          __nv_bfloat162 *pb = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            const float v0 = o_part[ch * 8 + 2 * i] + d[ch * 8 + 2 * i];
+            const float v1 = o_part[ch * 8 + 2 * i + 1] + d[ch * 8 + 2 * i + 1];
+            nonfinite |= !(isfinite(v0) && isfinite(v1));
+            pb[i] = __floats2bfloat162_rn(v0, v1);
+          }
+          *reinterpret_cast<uint4 *>(orow + ch * 8) = pk;
+        }
+      }
+    };
 
     for (int c = 0; c < nchunks; c++) {
       const int s = c % NST;
-      const int t0 = start + c * C;
-      const int L = min(C, end - t0);
       const float *coef = reinterpret_cast<const float *>(sm + SM::kCoef + s * SM::NCOEF * 4);
       mbar_wait(bar_ready + 8 * s, (c / NST) & 1, abort_flag);
 
@@ -193,44 +227,37 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         if (t < C) beta_r = coef[t];
         if (t < DK) dec = coef[C + t];
       }
+      // the previous chunk's output, while this chunk's first product runs
+      if (query_warp && c > 0) output_rows(c - 1);
       mbar_wait(bar_mma1, c & 1, abort_flag);
       fence_after_sync();
 
-      if (warp * 32 < C) {
+      if (key_warp) {
         // key rows: Y = beta (V - gam X) -> fp16 image row t
         const unsigned char *vrow = sm + SM::kV + s * SM::VI + t * 128;
+        float x[NS];
+        lane_row(tD1, x);
 #pragma unroll
-        for (int j0 = 0; j0 < NS; j0 += 16) {
-          float x[16];
-          tmem_ld16(tD1 + lane_base + j0, x);
-          tmem_wait_ld();
-          uint4 pk[2];
+        for (int ch = 0; ch < NS / 8; ch++) {
+          const uint4 vv = *reinterpret_cast<const uint4 *>(vrow + ((ch ^ (t & 7)) << 4));
+          const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(&vv);
+          uint4 pk;
+          __half2 *ph = reinterpret_cast<__half2 *>(&pk);
 #pragma unroll
-          for (int h = 0; h < 2; h++) {
-            const int ch = j0 / 8 + h;
-            const uint4 vv = *reinterpret_cast<const uint4 *>(vrow + ((ch ^ (t & 7)) << 4));
-            const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(&vv);
-            __half2 *ph = reinterpret_cast<__half2 *>(&pk[h]);
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-              const float2 vf = __bfloat1622float2(vb[i]);
-              const float xa = GATE == 0 ? gam_r * x[8 * h + 2 * i] : x[8 * h + 2 * i];
-              const float xb = GATE == 0 ? gam_r * x[8 * h + 2 * i + 1] : x[8 * h + 2 * i + 1];
-              ph[i] = __floats2half2_rn(beta_r * (vf.x - xa), beta_r * (vf.y - xb));
-            }
+          for (int i = 0; i < 4; i++) {
+            const float2 vf = __bfloat1622float2(vb[i]);
+            const float xa = GATE == 0 ? gam_r * x[ch * 8 + 2 * i] : x[ch * 8 + 2 * i];
+            const float xb = GATE == 0 ? gam_r * x[ch * 8 + 2 * i + 1] : x[ch * 8 + 2 * i + 1];
+            ph[i] = __floats2half2_rn(beta_r * (vf.x - xa), beta_r * (vf.y - xb));
           }
-          *reinterpret_cast<uint4 *>(sm + SM::kY + mnmajor_chunk_off(t, j0 / 8, 64)) = pk[0];
-          *reinterpret_cast<uint4 *>(sm + SM::kY + mnmajor_chunk_off(t, j0 / 8 + 1, 64)) = pk[1];
+          *reinterpret_cast<uint4 *>(sm + SM::kY + mnmajor_chunk_off(t, ch, 64)) = pk;
         }
-      } else if (warp >= 2 && (warp - 2) * 32 < C) {
-        // query rows: partial output
+      } else if (query_warp) {
+        // query rows: partial output of this chunk
+        lane_row(tD1, o_part);
+        if constexpr (GATE == 0) {
 #pragma unroll
-        for (int j0 = 0; j0 < NS; j0 += 16) {
-          float x[16];
-          tmem_ld16(tD1 + lane_base + j0, x);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; i++) o_part[j0 + i] = GATE == 0 ? sgam_r * x[i] : x[i];
+          for (int i = 0; i < NS; i++) o_part[i] *= sgam_r;
         }
       }
       fence_proxy_async();
@@ -258,46 +285,17 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       if (t == 0) mbar_arrive(bar_empty + 8 * s);  // MMAs and reads of stage s are done
 
       if (t < DK) {
+        float d[NS];
+        lane_row(tD2, d);
 #pragma unroll
-        for (int j0 = 0; j0 < NS; j0 += 16) {
-          float d[16];
-          tmem_ld16(tD2 + lane_base + j0, d);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; i++) s_reg[j0 + i] = fmaf(dec, s_reg[j0 + i], d[i]);
-        }
+        for (int i = 0; i < NS; i++) s_reg[i] = fmaf(dec, s_reg[i], d[i]);
         write_state_image();
-      }
-      if (warp >= 2 && (warp - 2) * 32 < C) {
-        const int r = t - 64;
-        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((long)(t0 + r) * a.HV + hv) * a.dv + col0;
-#pragma unroll
-        for (int j0 = 0; j0 < NS; j0 += 16) {
-          float d[16];
-          tmem_ld16(tD3 + lane_base + j0, d);
-          tmem_wait_ld();
-          uint4 pk[2];
-#pragma unroll
-          for (int h = 0; h < 2; h++) {
-            __nv_bfloat162 *pb = reinterpret_cast<__nv_bfloat162 *>(&pk[h]);
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-              const float v0 = o_part[j0 + 8 * h + 2 * i] + d[8 * h + 2 * i];
-              const float v1 = o_part[j0 + 8 * h + 2 * i + 1] + d[8 * h + 2 * i + 1];
-              nonfinite |= !(isfinite(v0) && isfinite(v1));
-              pb[i] = __floats2bfloat162_rn(v0, v1);
-            }
-          }
-          if (r < L) {
-            *reinterpret_cast<uint4 *>(orow + j0) = pk[0];
-            *reinterpret_cast<uint4 *>(orow + j0 + 8) = pk[1];
-          }
-        }
       }
       fence_proxy_async();
       fence_before_sync();
       named_bar(1, kChain);
     }
+    if (query_warp && nchunks > 0) output_rows(nchunks - 1);
 
     // ---- final state ----
     if (a.hT && t < DK) {
