@@ -74,6 +74,7 @@ struct Plan {
   long Ttot;      // packed token count
   long n_slots;   // chunk slots of the workspace
   size_t tile_bytes;
+  size_t kq_bytes;
   size_t ws_bytes;
 };
 
@@ -104,7 +105,11 @@ gdn_status plan(int B, int T, int H, int HV, int dk, int dv, int chunk,
   const size_t per = dtype == GDN_BF16 ? (size_t)gdn::kPrepImageBytes
                                        : 2u * (size_t)chunk * (size_t)chunk * sizeof(float);
   p.tile_bytes = (size_t)p.n_slots * (size_t)HV * per;
-  p.ws_bytes = gdn::kWorkspaceHeader + p.tile_bytes;
+  // bf16 scalar gate: the prep kernel also publishes the fp16 [K; Q] images
+  p.kq_bytes = (dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR)
+                   ? (size_t)p.n_slots * (size_t)H * (size_t)gdn::kq_image_bytes(dk)
+                   : 0;
+  p.ws_bytes = gdn::kWorkspaceHeader + p.tile_bytes + p.kq_bytes;
   return GDN_OK;
 }
 
@@ -188,6 +193,9 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
   seq.T = T;
   seq.Ttot = (int)p.Ttot;
   float *tiles = reinterpret_cast<float *>(static_cast<char *>(workspace) + gdn::kWorkspaceHeader);
+  unsigned char *kq_images =
+      p.kq_bytes ? static_cast<unsigned char *>(workspace) + gdn::kWorkspaceHeader + p.tile_bytes
+                 : nullptr;
 
   gdn::ScanMaps maps;
   if (dtype == GDN_BF16 &&
@@ -200,6 +208,7 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
       pa.q = q; pa.k = k; pa.g = g; pa.beta = beta;
       pa.seq = seq; pa.H = H; pa.HV = HV; pa.scale = scale;
       pa.tiles = tiles; pa.flags = flags; pa.n_slots = (int)p.n_slots;
+      pa.kq_images = kq_images;
       cudaError_t e;
       if (dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR)
         e = gdn::launch_prep_tmem(pa, maps, chunk, dk, stream);
@@ -214,7 +223,7 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
     gdn::ScanArgs sa;
     sa.q = q; sa.k = k; sa.v = v; sa.g = g; sa.beta = beta; sa.h0 = h0;
     sa.o = o; sa.hT = hT; sa.seq = seq; sa.H = H; sa.HV = HV; sa.dv = dv;
-    sa.scale = scale; sa.tiles = tiles; sa.flags = flags;
+    sa.scale = scale; sa.tiles = tiles; sa.flags = flags; sa.kq_images = kq_images;
     const cudaError_t e = dtype == GDN_BF16 ? gdn::launch_scan_tc(sa, maps, chunk, dk, gate_mode, stream)
                                             : gdn::launch_scan(sa, chunk, dk, dtype, gate_mode, stream);
     if (e != cudaSuccess) return GDN_ERR_CUDA;

@@ -18,6 +18,9 @@ constexpr int kScanTcSlice = 64;
 // (rows 0..127 = P1 = Kt^T T, rows 128..191 = Aqk T).
 constexpr int kPrepImageRows = 192;
 constexpr int kPrepImageBytes = kPrepImageRows * 128;
+// fp16 [K; Q] operand image of one (chunk, q/k head): 128 rows (keys at
+// 0..C-1, queries at 64..64+C-1), dk/64 panels of 128 x 128 bytes.
+__host__ __device__ constexpr int kq_image_bytes(int dk) { return (dk / 64) * 16384; }
 
 // Where packed sequence n starts: cu_seqlens[n], or n*T for plain batches.
 // Sequence n owns the chunk slots [floor(start_n / C) + n, ...): one slot per
@@ -38,6 +41,7 @@ struct PrepArgs {
   float *tiles;      // [n_slots][HV][2][C][C]: T = (I+A)^-1, then Aqk
   uint32_t *flags;   // device status word
   int n_slots;
+  unsigned char *kq_images;  // bf16 scalar-gate path: fp16 [K; Q] image per (slot, hq)
 };
 
 struct ScanArgs {
@@ -50,6 +54,7 @@ struct ScanArgs {
   float scale;
   const float *tiles;
   uint32_t *flags;
+  const unsigned char *kq_images;  // as PrepArgs::kq_images (read by the scan)
 };
 
 // Status-word bits (same values as GDN_FLAG_* in include/gdn.h).

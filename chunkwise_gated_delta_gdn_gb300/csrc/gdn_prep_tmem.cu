@@ -171,6 +171,13 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tslot;
+  // the first value head of each q/k group publishes the fp16 [K; Q] image for
+  // the scan kernel (same layout as its shared-memory operand)
+  if (hv % (a.HV / a.H) == 0) {
+    constexpr int KQB = kq_image_bytes(DK);
+    uint4 *dst = reinterpret_cast<uint4 *>(a.kq_images + ((size_t)slot * a.H + hq) * KQB);
+    for (int i = tid; i < KQB / 16; i += kThreads) dst[i] = reinterpret_cast<const uint4 *>(kq)[i];
+  }
 
   // ---- G = [K; Q] K^T ----
   if (tid == 0) {

@@ -65,7 +65,9 @@ struct ScanTcSmem {
   static constexpr int kBar = kCoef + NST * NCOEF * 4;
   static constexpr int kMisc = kBar + (3 * NST + 2) * 8;
   static constexpr int kBytes = kMisc + 16 + 1024;  // + alignment slack
-  static constexpr uint32_t kTx = 2 * C * DK * 2 + C * NS * 2 + PI;
+  // bytes landing per chunk: [Kg; Qg] (GDN: the prep's fp16 image; KDA: two
+  // TMA boxes per panel), the V slice and the prep image
+  static constexpr uint32_t kTx = (GATE == 0 ? KQ : 2 * C * DK * 2) + C * NS * 2 + PI;
   static_assert(KQ % 1024 == 0 && PI % 1024 == 0 && VI % 1024 == 0 && SI % 1024 == 0,
                 "1024-byte operand alignment");
   static_assert(kBytes <= 232448, "shared memory budget of one CTA");
@@ -323,10 +325,15 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       if (pt == 0) {
         mbar_arrive_expect_tx(full, SM::kTx);
         const uint32_t kq = smem_addr(sm + SM::kKQ + s * SM::KQ);
+        if constexpr (GATE == 0) {
+          // fp16 [K; Q] image written by the prep kernel
+          bulk_g2s(kq, a.kq_images + ((size_t)(base + c) * a.H + hq) * SM::KQ, SM::KQ, full);
+        } else {
 #pragma unroll
-        for (int p = 0; p < DK / 64; p++) {
-          tma_load_3d(kq + p * 16384, &maps.k, p * 64, hq, t0, full);
-          tma_load_3d(kq + p * 16384 + 64 * 128, &maps.q, p * 64, hq, t0, full);
+          for (int p = 0; p < DK / 64; p++) {
+            tma_load_3d(kq + p * 16384, &maps.k, p * 64, hq, t0, full);
+            tma_load_3d(kq + p * 16384 + 64 * 128, &maps.q, p * 64, hq, t0, full);
+          }
         }
         tma_load_3d(smem_addr(sm + SM::kV + s * SM::VI), &maps.v, col0, hv, t0, full);
         const unsigned char *src = reinterpret_cast<const unsigned char *>(a.tiles) +
@@ -367,24 +374,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       float *raw = reinterpret_cast<float *>(sm + SM::kRaw + s * SM::NRAW * 4);
       float *coef = reinterpret_cast<float *>(sm + SM::kCoef + s * SM::NCOEF * 4);
       if constexpr (GATE == 0) {
-        // keys and queries: bf16 -> fp16 in place; rows of the next sequence -> 0
-        constexpr int CH = (DK / 64) * 2 * C * 8;  // 16-byte chunks holding data
-        for (int idx = pt; idx < CH; idx += kChain) {
-          const int p = idx / (2 * C * 8), rem = idx % (2 * C * 8);
-          const int half = rem / (C * 8), r = (rem / 8) % C, chunk = rem % 8;
-          uint4 *ptr = reinterpret_cast<uint4 *>(kq + p * 16384 + (half * 64 + r) * 128 + chunk * 16);
-          uint4 v = *ptr, out = make_uint4(0, 0, 0, 0);
-          if (r < L) {
-            const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&v);
-            __half2 *h = reinterpret_cast<__half2 *>(&out);
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-              const float2 f = __bfloat1622float2(b[i]);
-              h[i] = __floats2half2_rn(f.x, f.y);
-            }
-          }
-          *ptr = out;
-        }
+        // keys and queries arrived as fp16 already; only the gate coefficients
         if (pt < 32) {
           const int lane = pt;
           const float g0 = lane < C ? raw[lane] : 0.f;
