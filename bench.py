@@ -341,7 +341,13 @@ def main():
     kbytes = algorithmic_bytes(wl, dominant)
     achieved = kbytes / (kern_ms / 1e3) / 1e9
     traffic, traffic_note = measured_traffic(c0.name, dominant, c0.tokens)
-    roofline = {"bound": "hbm", "kernel": f"gdn_{dominant}_kernel", "achieved": achieved,
+    kernel_names = {  # kernels gdn_chunk_fwd launches for this workload
+        ("prep", "bf16", 0): "gdn_prep_tmem_kernel", ("scan", "bf16", 0): "gdn_scan_tc_kernel",
+        ("prep", "bf16", 1): "gdn_prep_tc_kernel", ("scan", "bf16", 1): "gdn_scan_tc_kernel",
+        ("prep", "f32", 0): "gdn_prep_kernel", ("scan", "f32", 0): "gdn_scan_kernel",
+        ("prep", "f32", 1): "gdn_prep_kernel", ("scan", "f32", 1): "gdn_scan_kernel"}
+    roofline = {"bound": "hbm", "kernel": kernel_names[(dominant, wl.dtype_name, c0.gate_mode)],
+                "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic, "algorithmic_bytes": kbytes, "kernel_ms": kern_ms,
                 "peak_source": f"hbm_gbs of {peak_src}"}
