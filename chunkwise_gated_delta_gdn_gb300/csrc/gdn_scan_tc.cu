@@ -1,32 +1,34 @@
 // gdn_scan_tc.cu -- the serial-across-chunks scan kernel of the bf16 path, on
 // the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
-// One CTA per (sequence, value head, NS-column slice of dv), 256 threads:
-//  * warps 0-3 (the chain): thread t owns tensor-memory lane t and state row t
-//    (key channel t).  The fp32 state slice S (dk x NS) lives in registers for
-//    the whole sequence (register-resident state, stratat pull #1296, "What
-//    this is"); an fp16 copy in shared memory is the B operand of the products
-//    with S.  Per chunk (C rows, P1 and AqkT from the prep kernel's image):
-//       D1 = [Kg; Qg] S                 one M=128 MMA (rows 0..63 keys,
-//                                       64..127 queries), K = dk
-//       Y  = diag(beta) (V - D1[keys])  -> fp16 B operand
-//       D2 = P1 Y                       S <- diag(exp(b_last)) S + D2
-//       D3 = AqkT Y                     O  = D1[queries] + D3 -> o
-//    Two tensor-core round trips per chunk sit on the serial path; the O
-//    products ride along.
-//  * warps 4-7 (the producer) keep NST chunks in flight: one thread issues TMA
-//    tile loads of the chunk's keys, queries (two 64-column panels each) and V
-//    slice straight into the 128-byte-swizzled operand layout, plus a bulk copy
-//    of the prep image; all threads fetch gates and beta with cp.async.  Once a
-//    chunk has landed they convert keys and queries in place from bf16 to fp16
-//    (gated per channel for KDA), form the per-row gate coefficients, and
-//    publish the chunk to the chain.
-// The split over dv slices manufactures the parallelism a (batch, head) grid
-// lacks (ROCm/rocm-libraries PR #11223, "Notes for reviewers").  Operands are
-// fp16 (11-bit mantissa) with fp32 accumulation; the state itself stays fp32.
-// Every wait is bounded: a wait that runs out sets a status flag, after which
-// all waits return at once and the kernel finishes with the same control flow
-// in every thread (no hang, tensor memory freed).
+// One CTA per (sequence, value head, NS-column slice of dv), 384 threads:
+//  * warps 0-7 (the chain): warp w owns tensor-memory lanes / state rows
+//    32 (w % 4) .. +31 (key channels) and columns 32 (w / 4) .. +31 of the
+//    slice.  The fp32 state slice S (dk x NS) lives in registers for the whole
+//    sequence (register-resident state, stratat pull #1296, "What this is");
+//    an fp16 copy in shared memory is the B operand of the products with S.
+//    Per chunk c (C rows, P1 and AqkT from the prep kernel's image):
+//       D1[c&1] = [Kg; Qg] S          one M=128 MMA (rows 0..63 keys,
+//                                     64..127 queries), K = dk
+//       Y       = diag(beta)(V - gam D1[keys])   -> fp16 B operand Y[c&1]
+//       D2      = P1 Y                S <- diag(exp(b_last)) S + D2
+//       D3      = AqkT Y              issued right behind D2; it runs during
+//                                     the state update, off the serial path
+//       O       = scale gam D1[queries] + D3     -> o, during D1 of chunk c+1
+//    Two tensor-core round trips per chunk sit on the serial path.
+//  * warps 8-11 (the producer) keep NST chunks in flight: one thread issues
+//    bulk copies of the chunk's fp16 [Kg; Qg] image (GDN: written by the prep
+//    kernel) and of the prep image (KDA: TMA tile loads of the bf16 keys and
+//    queries, converted and gated per channel in place); all fetch gates and
+//    beta with cp.async and form the per-row gate coefficients.
+// V arrives by TMA into a two-deep ring of its own, two chunks ahead of its
+// use (issued by the chain as soon as a buffer has been consumed).  The split
+// over dv slices manufactures the parallelism a (batch, head) grid lacks
+// (ROCm/rocm-libraries PR #11223, "Notes for reviewers").
+// Operands are fp16 (11-bit mantissa) with fp32 accumulation; the state itself
+// stays fp32.  Every wait is bounded: a wait that runs out sets a status flag,
+// after which all waits return at once and the kernel finishes with the same
+// control flow in every thread (no hang, tensor memory freed).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,34 +43,40 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 256;
-constexpr int kChain = 128;  // chain threads (warps 0-3)
+constexpr int kChain = 256;  // chain threads (warps 0-7)
+constexpr int kProd = 128;   // producer threads (warps 8-11)
+constexpr int kThreads = kChain + kProd;
 constexpr int NS = kScanTcSlice;
-static_assert(NS == 64, "one 128-byte swizzle atom per V / S / Y row");
+constexpr int NH = NS / 2;  // columns per chain thread
+static_assert(NS == 64, "one 128-byte swizzle atom per S / Y row");
 
 template <int C, int DK, int GATE, int NST>
 struct ScanTcSmem {
   static constexpr int KQ = (DK / 64) * 128 * 128;  // [Kg; Qg], K-major, 128 rows
   static constexpr int PI = kPrepImageBytes;         // [P1; AqkT]
-  static constexpr int VI = C * 128;                 // V slice, C rows of 64 bf16
   static constexpr int SI = (DK / 8) * 1024;         // S, MN-major, dk K-rows
-  static constexpr int YI = 8 * 1024;                // Y, MN-major, 64 K-rows
+  static constexpr int YI = 8 * 1024;                // Y, MN-major, 64 K-rows (x2)
   static constexpr int NRAW = GATE == 0 ? 2 * C : C * DK + C;  // gates, beta
   static constexpr int NCOEF = GATE == 0 ? 3 * C + 4 : C + DK;
   static constexpr int kKQ = 0;
   static constexpr int kP = kKQ + NST * KQ;
-  static constexpr int kV = kP + NST * PI;
-  static constexpr int kS = kV + NST * VI;
+  static constexpr int kS = kP + NST * PI;
   static constexpr int kY = kS + SI;
-  static constexpr int kRaw = kY + YI;
+  static constexpr int VI = C * 128;                 // V slice, C rows x 64 bf16 (x2)
+  static constexpr int kV = kY + 2 * YI;
+  static constexpr int kRaw = kV + 2 * VI;
   static constexpr int kCoef = kRaw + NST * NRAW * 4;
   static constexpr int kBar = kCoef + NST * NCOEF * 4;
-  static constexpr int kMisc = kBar + (3 * NST + 2) * 8;
-  static constexpr int kBytes = kMisc + 16 + 1024;  // + alignment slack
-  // bytes landing per chunk: [Kg; Qg] (GDN: the prep's fp16 image; KDA: two
-  // TMA boxes per panel), the V slice and the prep image
-  static constexpr uint32_t kTx = (GATE == 0 ? KQ : 2 * C * DK * 2) + C * NS * 2 + PI;
-  static_assert(KQ % 1024 == 0 && PI % 1024 == 0 && VI % 1024 == 0 && SI % 1024 == 0,
+  static constexpr int kMisc = kBar + (3 * NST + 5) * 8;
+  static constexpr int kUsed = kMisc + 16;
+  // request 1 KB of alignment slack when it fits; otherwise the kernel checks
+  // that the dynamic shared memory it received is already 1 KB aligned
+  static constexpr int kSlack = kUsed + 1024 <= 232448 ? 1024 : 0;
+  static constexpr int kBytes = kUsed + kSlack;
+  // bytes landing per chunk: [Kg; Qg] (GDN: the prep's image; KDA: two TMA
+  // boxes per panel) and the prep image
+  static constexpr uint32_t kTx = (GATE == 0 ? KQ : 2 * C * DK * 2) + PI;
+  static_assert(KQ % 1024 == 0 && PI % 1024 == 0 && SI % 1024 == 0 && VI % 1024 == 0,
                 "1024-byte operand alignment");
   static_assert(kBytes <= 232448, "shared memory budget of one CTA");
 };
@@ -80,18 +88,23 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (sm - smem_raw > SM::kSlack) {  // dynamic shared memory not aligned as needed
+    if (tid == 0) atomicOr(a.flags, kFlagTimeout);
+    return;
+  }
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::kBar);
-  // bars: full[NST] (data landed), ready[NST] (converted), empty[NST] (consumed),
-  //       mma1, mma2
+  // bars: full[NST] (data landed), ready[NST] (published), empty[NST]
+  //       (consumed), mma1, mma2, mma3, vfull[2]
   const uint32_t bar_full = smem_addr(bars), bar_ready = smem_addr(bars + NST);
   const uint32_t bar_empty = smem_addr(bars + 2 * NST);
-  const uint32_t bar_mma1 = smem_addr(bars + 3 * NST), bar_mma2 = smem_addr(bars + 3 * NST + 1);
+  const uint32_t bar_mma1 = smem_addr(bars + 3 * NST), bar_mma2 = bar_mma1 + 8, bar_mma3 = bar_mma1 + 16;
+  const uint32_t bar_v = bar_mma1 + 24;  // two V buffers
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SM::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SM::kMisc + 4);
 
   const int n = blockIdx.x, hv = blockIdx.y, col0 = blockIdx.z * NS;
   const int hq = hv / (a.HV / a.H);
-  const int tid = threadIdx.x, warp = tid >> 5;
 
   int start, end;
   bool ok = seq_ok(a.seq, n, start, end);
@@ -106,57 +119,75 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   // ---- set-up: barriers, tensor memory, zero rows no load ever writes ----
   if (tid == 0) {
     for (int s = 0; s < NST; s++) {
-      mbar_init(bar_full + 8 * s, kChain + 1);
-      mbar_init(bar_ready + 8 * s, kChain);
+      mbar_init(bar_full + 8 * s, kProd + 1);
+      mbar_init(bar_ready + 8 * s, kProd);
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_mma1, 1);
     mbar_init(bar_mma2, 1);
+    mbar_init(bar_mma3, 1);
+    mbar_init(bar_v, 1);
+    mbar_init(bar_v + 8, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  constexpr uint32_t kTmemCols = 256;  // D1, D2, D3: 3 x NS columns
+  constexpr uint32_t kTmemCols = 256;  // D1 x2, D2, D3: 4 x NS columns
   if (warp == 0) tmem_alloc(smem_addr(tslot), kTmemCols);
-  for (int i = tid; i < (NST * SM::KQ) / 16; i += kThreads)
-    reinterpret_cast<uint4 *>(sm + SM::kKQ)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = tid; i < SM::YI / 16; i += kThreads)
+  if (GATE != 0) {
+    for (int i = tid; i < (NST * SM::KQ) / 16; i += kThreads)
+      reinterpret_cast<uint4 *>(sm + SM::kKQ)[i] = make_uint4(0, 0, 0, 0);
+  }
+  for (int i = tid; i < (2 * SM::YI) / 16; i += kThreads)
     reinterpret_cast<uint4 *>(sm + SM::kY)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tslot;
-  const uint32_t tD1 = tmem, tD2 = tmem + NS, tD3 = tmem + 2 * NS;
+  const uint32_t tD1 = tmem, tD2 = tmem + 2 * NS, tD3 = tmem + 3 * NS;
 
-  if (warp < 4) {
+  if (warp < 8) {
     // =====================================================================
     // chain
     // =====================================================================
-    const int t = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    float s_reg[NS];
+    const int q = warp & 3, hh = warp >> 2;
+    const int t = q * 32 + lane;        // tensor-memory lane = state row / chunk row
+    const int c0 = hh * NH;             // first column of this thread
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const bool key_warp = q * 32 < C;                       // lanes of key rows
+    const bool query_warp = q >= 2 && (q - 2) * 32 < C;     // lanes of query rows
+    const bool state_warp = q * 32 < DK;
+    float s_reg[NH];
     const size_t hoff = ((size_t)n * a.HV + hv) * (size_t)DK * a.dv;
-    if (t < DK) {
+    if (state_warp) {
 #pragma unroll
-      for (int j = 0; j < NS; j += 4) {
+      for (int j = 0; j < NH; j += 4) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.h0) v = __ldg(reinterpret_cast<const float4 *>(a.h0 + hoff + (size_t)t * a.dv + col0 + j));
+        if (a.h0) v = __ldg(reinterpret_cast<const float4 *>(a.h0 + hoff + (size_t)t * a.dv + col0 + c0 + j));
         s_reg[j] = v.x; s_reg[j + 1] = v.y; s_reg[j + 2] = v.z; s_reg[j + 3] = v.w;
       }
     }
     auto write_state_image = [&]() {
-      if (t < DK) {
 #pragma unroll
-        for (int ch = 0; ch < NS / 8; ch++) {
-          uint4 pk;
-          __half2 *h = reinterpret_cast<__half2 *>(&pk);
+      for (int ch = 0; ch < NH / 8; ch++) {
+        uint4 pk;
+        __half2 *h = reinterpret_cast<__half2 *>(&pk);
 #pragma unroll
-          for (int i = 0; i < 4; i++) h[i] = __floats2half2_rn(s_reg[ch * 8 + 2 * i], s_reg[ch * 8 + 2 * i + 1]);
-          *reinterpret_cast<uint4 *>(sm + SM::kS + mnmajor_chunk_off(t, ch, DK)) = pk;
-        }
+        for (int i = 0; i < 4; i++) h[i] = __floats2half2_rn(s_reg[ch * 8 + 2 * i], s_reg[ch * 8 + 2 * i + 1]);
+        *reinterpret_cast<uint4 *>(sm + SM::kS + mnmajor_chunk_off(t, c0 / 8 + ch, DK)) = pk;
       }
     };
-    write_state_image();
+    if (state_warp) write_state_image();
+    // V slice of chunk cc -> V buffer cc & 1 (TMA, issued by one thread)
+    auto issue_v = [&](int cc) {
+      const uint32_t bar = bar_v + 8 * (cc & 1);
+      mbar_arrive_expect_tx(bar, SM::VI);
+      tma_load_3d(smem_addr(sm + SM::kV + (cc & 1) * SM::VI), &maps.v, col0, hv, start + cc * C, bar);
+    };
+    if (tid == 0) {
+      if (nchunks > 0) issue_v(0);
+      if (nchunks > 1) issue_v(1);
+    }
     fence_proxy_async();
     fence_before_sync();
     named_bar(1, kChain);
@@ -164,36 +195,35 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     constexpr uint32_t idesc = idesc_f16(128, NS, 0, 1);
     const uint32_t sS = smem_addr(sm + SM::kS), sY = smem_addr(sm + SM::kY);
     bool nonfinite = false;
-    float o_part[NS];
-    const bool key_warp = warp * 32 < C;
-    const bool query_warp = warp >= 2 && (warp - 2) * 32 < C;
+    float sgam_prev = 0.f;  // scale * gam of this thread's query row, previous chunk
 
-    // all NS columns of this thread's lane at column `col` (one wait)
-    auto lane_row = [&](uint32_t col, float (&v)[NS]) {
-      uint32_t r0[32], r1[32];
-      tmem_ld32_nowait(col + lane_base, r0);
-      tmem_ld32_nowait(col + lane_base + 32, r1);
+    // the 32 columns of this thread's lane at tensor-memory column `col`
+    auto lane_half = [&](uint32_t col, float (&v)[NH]) {
+      uint32_t r[32];
+      tmem_ld32_nowait(col + lane_base + c0, r);
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; i++) { v[i] = __uint_as_float(r0[i]); v[32 + i] = __uint_as_float(r1[i]); }
+      for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
     };
-    // O of chunk cc = partial (Qg S) + AqkT Y, rounded to bf16 and stored
+    // O of chunk cc = scale gam Qg S (D1[cc&1], query lanes) + AqkT Y (D3)
     auto output_rows = [&](int cc) {
       const int r = t - 64;
       const int t0 = start + cc * C;
       const int L = min(C, end - t0);
-      float d[NS];
-      lane_row(tD3, d);
+      float qs[NH], d[NH];
+      lane_half(tD1 + (cc & 1) * NS, qs);
+      lane_half(tD3, d);
       if (r < L) {
-        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((long)(t0 + r) * a.HV + hv) * a.dv + col0;
+        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((long)(t0 + r) * a.HV + hv) * a.dv + col0 + c0;
 #pragma unroll
-        for (int ch = 0; ch < NS / 8; ch++) {
+        for (int ch = 0; ch < NH / 8; ch++) {
           uint4 pk;
           __nv_bfloat162 *pb = reinterpret_cast<__nv_bfloat162 *>(&pk);
 #pragma unroll
           for (int i = 0; i < 4; i++) {
-            const float v0 = o_part[ch * 8 + 2 * i] + d[ch * 8 + 2 * i];
-            const float v1 = o_part[ch * 8 + 2 * i + 1] + d[ch * 8 + 2 * i + 1];
+            const int j = ch * 8 + 2 * i;
+            const float v0 = (GATE == 0 ? sgam_prev * qs[j] : qs[j]) + d[j];
+            const float v1 = (GATE == 0 ? sgam_prev * qs[j + 1] : qs[j + 1]) + d[j + 1];
             nonfinite |= !(isfinite(v0) && isfinite(v1));
             pb[i] = __floats2bfloat162_rn(v0, v1);
           }
@@ -201,25 +231,34 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         }
       }
     };
+    auto issue_o_intra = [&](int cc) {  // D3 = AqkT Y[cc&1]
+      const uint32_t sP = smem_addr(sm + SM::kP + (cc % NST) * SM::PI);
+#pragma unroll
+      for (int k0 = 0; k0 < 64; k0 += 16) {
+        const uint64_t bd = make_desc(sY + (cc & 1) * SM::YI + (k0 >> 4) * 2048, 8 * 1024, 1024);
+        mma_f16(tD3, make_desc(sP + 64 * 128 + k0 * 2, 16, 1024), bd, idesc, k0 > 0 ? 1u : 0u);
+      }
+      mma_commit(bar_mma3);
+    };
 
     for (int c = 0; c < nchunks; c++) {
       const int s = c % NST;
       const float *coef = reinterpret_cast<const float *>(sm + SM::kCoef + s * SM::NCOEF * 4);
       mbar_wait(bar_ready + 8 * s, (c / NST) & 1, abort_flag);
 
-      // ---- D1 = [Kg; Qg] S ----
-      if (t == 0) {
+      // ---- D1[c&1] = [Kg; Qg] S; then the previous chunk's O-intra ----
+      if (tid == 0) {
         fence_after_sync();
         const uint32_t sKQ = smem_addr(sm + SM::kKQ + s * SM::KQ);
 #pragma unroll
         for (int k0 = 0; k0 < DK; k0 += 16) {
           const uint64_t ad = make_desc(sKQ + (k0 >> 6) * 16384 + (k0 & 63) * 2, 16, 1024);
           const uint64_t bd = make_desc(sS + (k0 >> 4) * 2048, (DK / 8) * 1024, 1024);
-          mma_f16(tD1, ad, bd, idesc, k0 > 0 ? 1u : 0u);
+          mma_f16(tD1 + (c & 1) * NS, ad, bd, idesc, k0 > 0 ? 1u : 0u);
         }
         mma_commit(bar_mma1);
       }
-      // coefficients (read before the stage is handed back)
+      // coefficients of this chunk (read before the stage is handed back)
       float beta_r = 0.f, gam_r = 0.f, sgam_r = 0.f, dec = 0.f;
       if constexpr (GATE == 0) {
         const int r = t & 63;
@@ -229,19 +268,26 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         if (t < C) beta_r = coef[t];
         if (t < DK) dec = coef[C + t];
       }
-      // the previous chunk's output, while this chunk's first product runs
-      if (query_warp && c > 0) output_rows(c - 1);
+      // the previous chunk's output and its stage, while D1 runs
+      if (c > 0) {
+        mbar_wait(bar_mma3, (c - 1) & 1, abort_flag);
+        fence_after_sync();
+        if (query_warp) output_rows(c - 1);
+        if (tid == 0) mbar_arrive(bar_empty + 8 * ((c - 1) % NST));
+      }
+      sgam_prev = sgam_r;
       mbar_wait(bar_mma1, c & 1, abort_flag);
       fence_after_sync();
 
       if (key_warp) {
-        // key rows: Y = beta (V - gam X) -> fp16 image row t
-        const unsigned char *vrow = sm + SM::kV + s * SM::VI + t * 128;
-        float x[NS];
-        lane_row(tD1, x);
+        // key rows: Y = beta (V - gam X) -> fp16 image row t, this thread's columns
+        float x[NH];
+        lane_half(tD1 + (c & 1) * NS, x);
+        mbar_wait(bar_v + 8 * (c & 1), (c >> 1) & 1, abort_flag);
+        const unsigned char *vrow = sm + SM::kV + (c & 1) * SM::VI + t * 128;
 #pragma unroll
-        for (int ch = 0; ch < NS / 8; ch++) {
-          const uint4 vv = *reinterpret_cast<const uint4 *>(vrow + ((ch ^ (t & 7)) << 4));
+        for (int ch = 0; ch < NH / 8; ch++) {
+          const uint4 vv = *reinterpret_cast<const uint4 *>(vrow + (((c0 / 8 + ch) ^ (t & 7)) << 4));
           const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(&vv);
           uint4 pk;
           __half2 *ph = reinterpret_cast<__half2 *>(&pk);
@@ -252,60 +298,53 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
             const float xb = GATE == 0 ? gam_r * x[ch * 8 + 2 * i + 1] : x[ch * 8 + 2 * i + 1];
             ph[i] = __floats2half2_rn(beta_r * (vf.x - xa), beta_r * (vf.y - xb));
           }
-          *reinterpret_cast<uint4 *>(sm + SM::kY + mnmajor_chunk_off(t, ch, 64)) = pk;
-        }
-      } else if (query_warp) {
-        // query rows: partial output of this chunk
-        lane_row(tD1, o_part);
-        if constexpr (GATE == 0) {
-#pragma unroll
-          for (int i = 0; i < NS; i++) o_part[i] *= sgam_r;
+          *reinterpret_cast<uint4 *>(sm + SM::kY + (c & 1) * SM::YI + mnmajor_chunk_off(t, c0 / 8 + ch, 64)) = pk;
         }
       }
       fence_proxy_async();
       fence_before_sync();
       named_bar(1, kChain);
 
-      // ---- D2 = P1 Y, D3 = AqkT Y ----
-      if (t == 0) {
+      // ---- D2 = P1 Y; V buffer c & 1 is free: fetch chunk c + 2 into it ----
+      if (tid == 0) {
         fence_after_sync();
+        if (c + 2 < nchunks) issue_v(c + 2);
         const uint32_t sP = smem_addr(sm + SM::kP + s * SM::PI);
 #pragma unroll
         for (int k0 = 0; k0 < 64; k0 += 16) {
-          const uint64_t bd = make_desc(sY + (k0 >> 4) * 2048, 8 * 1024, 1024);
+          const uint64_t bd = make_desc(sY + (c & 1) * SM::YI + (k0 >> 4) * 2048, 8 * 1024, 1024);
           mma_f16(tD2, make_desc(sP + k0 * 2, 16, 1024), bd, idesc, k0 > 0 ? 1u : 0u);
         }
-#pragma unroll
-        for (int k0 = 0; k0 < 64; k0 += 16) {
-          const uint64_t bd = make_desc(sY + (k0 >> 4) * 2048, 8 * 1024, 1024);
-          mma_f16(tD3, make_desc(sP + 64 * 128 + k0 * 2, 16, 1024), bd, idesc, k0 > 0 ? 1u : 0u);
-        }
         mma_commit(bar_mma2);
+        issue_o_intra(c);
       }
       mbar_wait(bar_mma2, c & 1, abort_flag);
       fence_after_sync();
-      if (t == 0) mbar_arrive(bar_empty + 8 * s);  // MMAs and reads of stage s are done
 
-      if (t < DK) {
-        float d[NS];
-        lane_row(tD2, d);
+      if (state_warp) {
+        float d[NH];
+        lane_half(tD2, d);
 #pragma unroll
-        for (int i = 0; i < NS; i++) s_reg[i] = fmaf(dec, s_reg[i], d[i]);
+        for (int i = 0; i < NH; i++) s_reg[i] = fmaf(dec, s_reg[i], d[i]);
         write_state_image();
       }
       fence_proxy_async();
       fence_before_sync();
       named_bar(1, kChain);
     }
-    if (query_warp && nchunks > 0) output_rows(nchunks - 1);
+    if (nchunks > 0) {
+      mbar_wait(bar_mma3, (nchunks - 1) & 1, abort_flag);
+      fence_after_sync();
+      if (query_warp) output_rows(nchunks - 1);
+    }
 
     // ---- final state ----
-    if (a.hT && t < DK) {
+    if (a.hT && state_warp) {
 #pragma unroll
-      for (int j = 0; j < NS; j += 4) {
+      for (int j = 0; j < NH; j += 4) {
         nonfinite |= !(isfinite(s_reg[j]) && isfinite(s_reg[j + 1]) && isfinite(s_reg[j + 2]) &&
                        isfinite(s_reg[j + 3]));
-        *reinterpret_cast<float4 *>(a.hT + hoff + (size_t)t * a.dv + col0 + j) =
+        *reinterpret_cast<float4 *>(a.hT + hoff + (size_t)t * a.dv + col0 + c0 + j) =
             make_float4(s_reg[j], s_reg[j + 1], s_reg[j + 2], s_reg[j + 3]);
       }
     }
@@ -335,7 +374,6 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
             tma_load_3d(kq + p * 16384 + 64 * 128, &maps.q, p * 64, hq, t0, full);
           }
         }
-        tma_load_3d(smem_addr(sm + SM::kV + s * SM::VI), &maps.v, col0, hv, t0, full);
         const unsigned char *src = reinterpret_cast<const unsigned char *>(a.tiles) +
                                    ((size_t)(base + c) * a.HV + hv) * kPrepImageBytes;
         bulk_g2s(smem_addr(sm + SM::kP + s * SM::PI), src, kPrepImageBytes, full);
@@ -349,7 +387,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
           cp_async4(smem_addr(raw + C + pt), a.beta + row * a.HV + hv, in ? 4u : 0u);
         }
       } else {
-        for (int idx = pt; idx < C * DK / 4; idx += kChain) {
+        for (int idx = pt; idx < C * DK / 4; idx += kProd) {
           const int r = idx / (DK / 4), c4 = (idx % (DK / 4)) * 4;
           const bool in = r < L;
           const long row = in ? (long)(t0 + r) : (long)t0;
@@ -364,7 +402,8 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       cp_async_arrive_noinc(full);
     };
 
-    // convert chunk c (landed) in place and publish it
+    // chunk c landed: gate coefficients (and for KDA the gated fp16 keys and
+    // queries), then publish it
     auto finish = [&](int c) {
       const int s = c % NST;
       const int t0 = start + c * C;
@@ -374,9 +413,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       float *raw = reinterpret_cast<float *>(sm + SM::kRaw + s * SM::NRAW * 4);
       float *coef = reinterpret_cast<float *>(sm + SM::kCoef + s * SM::NCOEF * 4);
       if constexpr (GATE == 0) {
-        // keys and queries arrived as fp16 already; only the gate coefficients
         if (pt < 32) {
-          const int lane = pt;
           const float g0 = lane < C ? raw[lane] : 0.f;
           const float g1 = lane + 32 < C ? raw[lane + 32] : 0.f;
           if (__any_sync(0xffffffffu, g0 > 0.f || g1 > 0.f) && lane == 0) atomicOr(a.flags, kFlagPositiveGate);
@@ -418,10 +455,10 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
           if (positive) atomicOr(a.flags, kFlagPositiveGate);
         }
         if (pt < C) coef[pt] = raw[C * DK + pt];
-        named_bar(2, kChain);
+        named_bar(2, kProd);
         // gated keys / queries: bf16 -> fp16 (k exp(b), scale q exp(b)) in place
         constexpr int CH = (DK / 64) * 2 * C * 8;
-        for (int idx = pt; idx < CH; idx += kChain) {
+        for (int idx = pt; idx < CH; idx += kProd) {
           const int p = idx / (2 * C * 8), rem = idx % (2 * C * 8);
           const int half = rem / (C * 8), r = (rem / 8) % C, chunk = rem % 8;
           const int row = half * 64 + r;
@@ -441,8 +478,8 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
           }
           *ptr = out;
         }
+        fence_proxy_async();
       }
-      fence_proxy_async();
       mbar_arrive(bar_ready + 8 * s);
     };
 
