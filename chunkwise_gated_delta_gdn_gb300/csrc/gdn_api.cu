@@ -101,11 +101,13 @@ gdn_status plan(int B, int T, int H, int HV, int dk, int dv, int chunk,
   p.n_slots = p.Ttot / chunk + p.n_states;
   if (p.n_slots > INT32_MAX) return GDN_ERR_UNSUPPORTED;
   // fp32 inputs: T and Aqk as fp32 C x C tiles; bf16 inputs: one fp16 operand
-  // image per (chunk, value head)
-  const size_t per = dtype == GDN_BF16 ? (size_t)gdn::kPrepImageBytes
-                                       : 2u * (size_t)chunk * (size_t)chunk * sizeof(float);
+  // image per (chunk, value head), [P1; E; AqkT] for the scalar gate and
+  // [P1; AqkT] for the per-key gate
+  size_t per = 2u * (size_t)chunk * (size_t)chunk * sizeof(float);
+  if (dtype == GDN_BF16)
+    per = gate_mode == GDN_GATE_SCALAR ? (size_t)gdn::kLaImageBytes : (size_t)gdn::kPrepImageBytes;
   p.tile_bytes = (size_t)p.n_slots * (size_t)HV * per;
-  // bf16 scalar gate: the prep kernel also publishes the fp16 [K; Q] images
+  // bf16 scalar gate: the prep kernel also publishes the [K_next; Q] images
   p.kq_bytes = (dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR)
                    ? (size_t)p.n_slots * (size_t)H * (size_t)gdn::kq_image_bytes(dk)
                    : 0;
@@ -224,8 +226,13 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
     sa.q = q; sa.k = k; sa.v = v; sa.g = g; sa.beta = beta; sa.h0 = h0;
     sa.o = o; sa.hT = hT; sa.seq = seq; sa.H = H; sa.HV = HV; sa.dv = dv;
     sa.scale = scale; sa.tiles = tiles; sa.flags = flags; sa.kq_images = kq_images;
-    const cudaError_t e = dtype == GDN_BF16 ? gdn::launch_scan_tc(sa, maps, chunk, dk, gate_mode, stream)
-                                            : gdn::launch_scan(sa, chunk, dk, dtype, gate_mode, stream);
+    cudaError_t e;
+    if (dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR)
+      e = gdn::launch_scan_la(sa, maps, chunk, dk, stream);
+    else if (dtype == GDN_BF16)
+      e = gdn::launch_scan_tc(sa, maps, chunk, dk, gate_mode, stream);
+    else
+      e = gdn::launch_scan(sa, chunk, dk, dtype, gate_mode, stream);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
   }
   return GDN_OK;

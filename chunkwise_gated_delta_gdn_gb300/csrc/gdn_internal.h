@@ -18,8 +18,16 @@ constexpr int kScanTcSlice = 64;
 // (rows 0..127 = P1 = Kt^T T, rows 128..191 = Aqk T).
 constexpr int kPrepImageRows = 192;
 constexpr int kPrepImageBytes = kPrepImageRows * 128;
-// fp16 [K; Q] operand image of one (chunk, q/k head): 128 rows (keys at
-// 0..C-1, queries at 64..64+C-1), dk/64 panels of 128 x 128 bytes.
+// The scalar-gate bf16 path's image (one-chunk lookahead): 256 rows x 64 fp16,
+// K-major with the 128-byte swizzle: rows 0..127 = P1 of the chunk, rows
+// 128..191 = E = K_next P1 (the next chunk's keys times this chunk's P1; zero
+// for a sequence's last chunk), rows 192..255 = Aqk T.
+constexpr int kLaImageRows = 256;
+constexpr int kLaImageBytes = kLaImageRows * 128;
+// The same path's key/query image of one (chunk, q/k head): the A operand
+// [K_next; Q] of the scan's state product, 128 rows of fp16 (next chunk's keys
+// at 0..C-1, zero for a sequence's last chunk; this chunk's queries at
+// 64..64+C-1), dk/64 panels of 128 x 128 bytes, K-major, 128-byte swizzle.
 __host__ __device__ constexpr int kq_image_bytes(int dk) { return (dk / 64) * 16384; }
 
 // Where packed sequence n starts: cu_seqlens[n], or n*T for plain batches.
@@ -41,7 +49,7 @@ struct PrepArgs {
   float *tiles;      // [n_slots][HV][2][C][C]: T = (I+A)^-1, then Aqk
   uint32_t *flags;   // device status word
   int n_slots;
-  unsigned char *kq_images;  // bf16 scalar-gate path: fp16 [K; Q] image per (slot, hq)
+  unsigned char *kq_images;  // bf16 scalar gate: [K_next; Q] image per (slot, hq)
 };
 
 struct ScanArgs {
@@ -78,13 +86,17 @@ struct ScanMaps {
 bool make_scan_maps(ScanMaps &m, const void *q, const void *k, const void *v, int Ttot,
                     int H, int HV, int dk, int dv, int chunk);
 
-// bf16 path: prep writing fp16 operand images, tcgen05 scan consuming them
+// bf16 per-key-gate path: prep writing fp16 operand images, tcgen05 scan
+// consuming them
 cudaError_t launch_prep_tc(const PrepArgs &a, int chunk, int dk, int gate,
                            cudaStream_t stream);
 cudaError_t launch_scan_tc(const ScanArgs &a, const ScanMaps &maps, int chunk, int dk,
                            int gate, cudaStream_t stream);
-// bf16 scalar-gate prep on tensor memory (same image as launch_prep_tc)
+// bf16 scalar-gate path: prep on tensor memory writing the lookahead image,
+// and the lookahead scan consuming it
 cudaError_t launch_prep_tmem(const PrepArgs &a, const ScanMaps &maps, int chunk, int dk,
                              cudaStream_t stream);
+cudaError_t launch_scan_la(const ScanArgs &a, const ScanMaps &maps, int chunk, int dk,
+                           cudaStream_t stream);
 
 }  // namespace gdn

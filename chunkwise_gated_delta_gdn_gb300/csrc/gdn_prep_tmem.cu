@@ -3,9 +3,10 @@
 //
 // One CTA per (chunk slot, q/k head), one warpgroup (128 threads) per value
 // head of the group (up to three at once).  The group shares the key/query
-// tile: it arrives once by TMA (bf16, 128-byte swizzle), is converted to fp16
-// in place, published for the scan kernel as its [K; Q] operand image, and
-// feeds one Gram product for all value heads:
+// tile and the next chunk's key tile: they arrive once by TMA (bf16, 128-byte
+// swizzle), are converted to fp16 in place, published for the scan kernel as
+// its [K_next; Q] operand image, and feed one Gram product for all value
+// heads:
 //   G  = [K; Q] K^T          M = 128 (keys then queries), N = C, K = dk
 // Each warpgroup then, for its value head (gates and beta differ per head):
 //   A    = strict-lower(beta_r G_rs exp(b_r - b_s)), Aqk = lower(scale P_rs
@@ -16,9 +17,13 @@
 //          rows by split-bf16 tensor-core products against the solved blocks
 //   P1   = K^T (D T)         the key tile read MN-major, D = diag(exp(b_last - b_s))
 //   AqkT = Aqk T
-// and writes P1 and AqkT, rounded once to fp16, as the 24 KB operand image of
-// the scan kernel (rows 0..127 = P1, rows 128..191 = AqkT; K-major, 128-byte
-// swizzle) straight from registers.
+//   E    = K_next P1         (fp16 P1 as the B operand; zero for the last chunk
+//                             of a sequence)
+// and writes them, each rounded once to fp16, as the 32 KB operand image of the
+// lookahead scan kernel (rows 0..127 = P1, 128..191 = E, 192..255 = AqkT;
+// K-major, 128-byte swizzle) straight from registers.  E lets the scan form
+// the next chunk's K S from this chunk's Y without waiting for the state:
+//   K_next S_next = exp(b_last) K_next S + E Y.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -44,9 +49,12 @@ __device__ __forceinline__ float ex2(float x) {
 template <int C, int NWG>
 struct PrepTmemSmem {
   static constexpr int LDC = C + 1;               // fp32 row stride of A / T (odd)
-  static constexpr int KQ = 2 * 128 * 128;        // [K; Q] image, always two panels
+  // [K; Q; K_next], K-major, always two panels of 192 rows x 128 bytes
+  static constexpr int PANEL = 192 * 128;
+  static constexpr int KQ = 2 * PANEL;
   // per warpgroup
   static constexpr int WG_AQK = 0;                // Aqk, K-major, 64 rows (8 KB)
+  static constexpr int WG_P1 = 0;                 // later: P1, MN-major, dk K-rows (16 KB)
   static constexpr int WG_TI = 8 * 1024;          // T, MN-major, 64 K-rows (8 KB)
   static constexpr int WG_DTI = 16 * 1024;        // D T, MN-major (8 KB)
   static constexpr int WG_A = 24 * 1024;          // A -> T, fp32
@@ -100,6 +108,8 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     meta[0] = valid ? (int)t0 : 0;
     meta[1] = valid ? (int)min((long)C, (long)end - t0) : 0;
     meta[2] = valid;
+    // tokens of the sequence's next chunk (0 for its last chunk)
+    meta[3] = (valid && t0 + C < end) ? (int)min((long)C, (long)end - t0 - C) : 0;
     *abort_flag = 0;
     if (valid) {
       mbar_init(bar_tma, 1);
@@ -110,35 +120,36 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   }
   __syncthreads();
   if (!meta[2]) return;  // unused slot: the scan never reads it
-  const int t0 = meta[0], L = meta[1];
+  const int t0 = meta[0], L = meta[1], Ln = meta[3];
 
   if (warp == 0) tmem_alloc(smem_addr(tslot), 512);
   if (C < 64) {  // zero the rows no TMA box covers
     for (int i = tid; i < SM::KQ / 16; i += NT) {
-      const int row = (i * 16 % 16384) / 128;
+      const int row = (i * 16 % SM::PANEL) / 128;
       if ((row & 63) >= C) reinterpret_cast<uint4 *>(kq)[i] = make_uint4(0, 0, 0, 0);
     }
   }
   fence_proxy_async();
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar_tma, 2 * C * DK * 2);
+    mbar_arrive_expect_tx(bar_tma, (Ln > 0 ? 3 : 2) * C * DK * 2);
 #pragma unroll
     for (int p = 0; p < DK / 64; p++) {
-      tma_load_3d(smem_addr(kq + p * 16384), &maps.k, p * 64, hq, t0, bar_tma);
-      tma_load_3d(smem_addr(kq + p * 16384 + 64 * 128), &maps.q, p * 64, hq, t0, bar_tma);
+      tma_load_3d(smem_addr(kq + p * SM::PANEL), &maps.k, p * 64, hq, t0, bar_tma);
+      tma_load_3d(smem_addr(kq + p * SM::PANEL + 64 * 128), &maps.q, p * 64, hq, t0, bar_tma);
+      if (Ln > 0) tma_load_3d(smem_addr(kq + p * SM::PANEL + 128 * 128), &maps.k, p * 64, hq, t0 + C, bar_tma);
     }
   }
   mbar_wait(bar_tma, 0, abort_flag);
-  // bf16 -> fp16 in place; rows beyond the chunk's tokens -> 0
+  // bf16 -> fp16 in place; rows beyond each tile's tokens -> 0
   {
-    constexpr int CH = (DK / 64) * 2 * C * 8;
+    constexpr int CH = (DK / 64) * 3 * C * 8;
     for (int idx = tid; idx < CH; idx += NT) {
-      const int p = idx / (2 * C * 8), rem = idx % (2 * C * 8);
-      const int half = rem / (C * 8), r = (rem / 8) % C, chunk = rem % 8;
-      uint4 *ptr = reinterpret_cast<uint4 *>(kq + p * 16384 + (half * 64 + r) * 128 + chunk * 16);
-      const uint4 v = *ptr;
+      const int p = idx / (3 * C * 8), rem = idx % (3 * C * 8);
+      const int third = rem / (C * 8), r = (rem / 8) % C, chunk = rem % 8;
+      uint4 *ptr = reinterpret_cast<uint4 *>(kq + p * SM::PANEL + (third * 64 + r) * 128 + chunk * 16);
       uint4 out = make_uint4(0, 0, 0, 0);
-      if (r < L) {
+      if (r < (third == 2 ? Ln : L)) {
+        const uint4 v = *ptr;
         const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&v);
         __half2 *h = reinterpret_cast<__half2 *>(&out);
 #pragma unroll
@@ -161,16 +172,20 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     constexpr uint32_t id = idesc_f16(128, C, 0, 0);
 #pragma unroll
     for (int k0 = 0; k0 < DK; k0 += 16) {
-      const uint64_t d = make_desc(sKQ + (k0 >> 6) * 16384 + (k0 & 63) * 2, 16, 1024);
+      const uint64_t d = make_desc(sKQ + (k0 >> 6) * SM::PANEL + (k0 & 63) * 2, 16, 1024);
       mma_f16(tmem, d, d, id, k0 > 0 ? 1u : 0u);  // B = the key rows of the same image
     }
     mma_commit(bar_gram);
   }
-  // publish the fp16 [K; Q] image for the scan kernel while the Gram runs
+  // publish [K_next; Q] (rows 128.. and 64.. of each panel) while the Gram runs
   {
     constexpr int KQB = kq_image_bytes(DK);
     uint4 *dst = reinterpret_cast<uint4 *>(a.kq_images + ((size_t)slot * a.H + hq) * KQB);
-    for (int i = tid; i < KQB / 16; i += NT) dst[i] = reinterpret_cast<const uint4 *>(kq)[i];
+    for (int i = tid; i < KQB / 16; i += NT) {
+      const int p = i >> 10, within = (i & 1023) * 16;  // 16 KB per image panel
+      const int from = p * SM::PANEL + (within < 8192 ? 16384 + within : within);
+      dst[i] = *reinterpret_cast<const uint4 *>(kq + from);
+    }
   }
 
   // ---- per value head, one warpgroup each ----
@@ -183,9 +198,9 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   const uint32_t bar_mma = bar_tma + 16 + 8 * wg;
   const uint32_t tP1 = tmem + 64 + 128 * wg, tAT = tP1 + 64;
   const int wlane0 = (warp & 3) * 32;  // first tensor-memory lane of this warp
-  int round = 0;
+  int mma_uses = 0;  // completions of bar_mma so far
   bool first = true;
-  for (int j = wg; j < G; j += NWG, round++) {
+  for (int j = wg; j < G; j += NWG) {
     const int hv = hq * G + j;
     // gates (log2 units), beta, cumulative gates, end-of-chunk decays
     bool positive = false;
@@ -340,7 +355,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       constexpr uint32_t idQ = idesc_f16(128, C, 0, 1);
 #pragma unroll
       for (int k0 = 0; k0 < C; k0 += 16) {
-        mma_f16(tP1, make_desc(sKQ + k0 * 128, 16384, 1024),
+        mma_f16(tP1, make_desc(sKQ + k0 * 128, SM::PANEL, 1024),
                 make_desc(sDT + (k0 >> 4) * 2048, 8192, 1024), idP, k0 > 0 ? 1u : 0u);
       }
 #pragma unroll
@@ -350,13 +365,16 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       }
       mma_commit(bar_mma);
     }
-    mbar_wait(bar_mma, round & 1, abort_flag);
+    mbar_wait(bar_mma, mma_uses++ & 1, abort_flag);
     fence_after_sync();
 
-    // ---- the image, straight to HBM: row t <- P1 row t, row 128 + t <- AqkT row t ----
+    // ---- the image, straight to HBM from the tensor-memory lanes ----
     unsigned char *img = reinterpret_cast<unsigned char *>(a.tiles) +
-                         ((size_t)slot * a.HV + hv) * kPrepImageBytes;
-    auto put_row = [&](int row, uint32_t taddr, bool have) {
+                         ((size_t)slot * a.HV + hv) * kLaImageBytes;
+    // image row `row` <- this lane's row at `taddr` (zeros when !have); with
+    // `mn`, the fp16 row also goes to shared memory as K-row t of an MN-major
+    // image (the B operand of E)
+    auto put_row = [&](int row, uint32_t taddr, bool have, unsigned char *mn) {
 #pragma unroll
       for (int h = 0; h < 2; h++) {  // 32 columns at a time
         uint32_t v[32];
@@ -375,12 +393,35 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
             const float f1 = load ? __uint_as_float(v[ch * 8 + 2 * i + 1]) : 0.f;
             hh[i] = __floats2half2_rn(f0, f1);
           }
-          *reinterpret_cast<uint4 *>(img + kmajor_off(row, 32 * h + ch * 8, kPrepImageRows)) = pk;
+          *reinterpret_cast<uint4 *>(img + kmajor_off(row, 32 * h + ch * 8, kLaImageRows)) = pk;
+          if (mn && 32 * h < C) *reinterpret_cast<uint4 *>(mn + mnmajor_chunk_off(t, 4 * h + ch, DK)) = pk;
         }
       }
     };
-    put_row(t, tP1 + lane_base, wlane0 < DK);
-    if (t < 64) put_row(128 + t, tAT + lane_base, wlane0 < C);
+    if (t < 64) put_row(192 + t, tAT + lane_base, wlane0 < C, nullptr);
+    put_row(t, tP1 + lane_base, wlane0 < DK, t < DK ? ws + SM::WG_P1 : nullptr);
+    fence_proxy_async();
+    fence_before_sync();
+    named_bar(1 + wg, 128);
+    fence_after_sync();
+
+    // ---- E = K_next P1 (M = 128 rows from the next-key tile, N = C, K = dk),
+    //      into the Aqk T columns that were just read out ----
+    if (Ln > 0) {
+      if (t == 0) {
+        const uint32_t sKn = smem_addr(kq) + 128 * 128, sP1 = smem_addr(ws + SM::WG_P1);
+        constexpr uint32_t idE = idesc_f16(128, C, 0, 1);
+#pragma unroll
+        for (int k0 = 0; k0 < DK; k0 += 16) {
+          mma_f16(tAT, make_desc(sKn + (k0 >> 6) * SM::PANEL + (k0 & 63) * 2, 16, 1024),
+                  make_desc(sP1 + (k0 >> 4) * 2048, (DK / 8) * 1024, 1024), idE, k0 > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_mma);
+      }
+      mbar_wait(bar_mma, mma_uses++ & 1, abort_flag);
+      fence_after_sync();
+    }
+    if (t < 64) put_row(128 + t, tAT + lane_base, Ln > 0 && wlane0 < C, nullptr);
     fence_before_sync();
     named_bar(1 + wg, 128);
   }

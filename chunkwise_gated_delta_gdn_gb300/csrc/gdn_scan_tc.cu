@@ -364,15 +364,10 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       if (pt == 0) {
         mbar_arrive_expect_tx(full, SM::kTx);
         const uint32_t kq = smem_addr(sm + SM::kKQ + s * SM::KQ);
-        if constexpr (GATE == 0) {
-          // fp16 [K; Q] image written by the prep kernel
-          bulk_g2s(kq, a.kq_images + ((size_t)(base + c) * a.H + hq) * SM::KQ, SM::KQ, full);
-        } else {
 #pragma unroll
-          for (int p = 0; p < DK / 64; p++) {
-            tma_load_3d(kq + p * 16384, &maps.k, p * 64, hq, t0, full);
-            tma_load_3d(kq + p * 16384 + 64 * 128, &maps.q, p * 64, hq, t0, full);
-          }
+        for (int p = 0; p < DK / 64; p++) {
+          tma_load_3d(kq + p * 16384, &maps.k, p * 64, hq, t0, full);
+          tma_load_3d(kq + p * 16384 + 64 * 128, &maps.q, p * 64, hq, t0, full);
         }
         const unsigned char *src = reinterpret_cast<const unsigned char *>(a.tiles) +
                                    ((size_t)(base + c) * a.HV + hv) * kPrepImageBytes;
@@ -511,9 +506,10 @@ cudaError_t launch_one(const ScanArgs &a, const ScanMaps &maps, cudaStream_t str
 
 template <int C, int DK>
 cudaError_t dispatch_gate(const ScanArgs &a, const ScanMaps &m, int gate, cudaStream_t s) {
-  // three stages in flight where shared memory allows (GDN), two for KDA,
-  // whose per-channel gates take a stage's worth of room
-  return gate ? launch_one<C, DK, 1, 2>(a, m, s) : launch_one<C, DK, 0, 3>(a, m, s);
+  // the scalar gate runs the lookahead scan (gdn_scan_la.cu); two stages in
+  // flight for the per-key gate, whose per-channel gates take a stage's room
+  if (!gate) return cudaErrorInvalidValue;
+  return launch_one<C, DK, 1, 2>(a, m, s);
 }
 
 }  // namespace

@@ -46,11 +46,12 @@ def test_status_strings(lib):
 
 
 def test_workspace_query(lib):
-    # bf16, scalar gate: header + (T/C + N) slots x (HV x one 24 KB fp16 operand
-    # image + H x one 32 KB fp16 [K; Q] image)
+    # bf16, scalar gate: header + (T/C + N) slots x (HV x one 32 KB fp16 operand
+    # image [P1; E; AqkT] + H x one 32 KB fp16 [K_next; Q] image)
     ws = gdn.gdn_chunk_fwd_workspace_bytes(1, 32768, 16, 48, 128, 128, 64, 0, 1, gdn.GDN_BF16)
-    assert ws == 256 + (32768 // 64 + 1) * (48 * 192 * 128 + 16 * 2 * 128 * 128)
-    # bf16, per-key gate: no [K; Q] images
+    assert ws == 256 + (32768 // 64 + 1) * (48 * 256 * 128 + 16 * 2 * 128 * 128)
+    # bf16, per-key gate: one 24 KB image [P1; AqkT] per (slot, value head), no
+    # key/query images
     ws = gdn.gdn_chunk_fwd_workspace_bytes(2, 8192, 32, 32, 128, 128, 32, 1, 2, gdn.GDN_BF16)
     assert ws == 256 + (2 * 8192 // 32 + 2) * 32 * 192 * 128
     # fp32: header + slots x HV x (T and Aqk, C x C fp32)
