@@ -165,6 +165,46 @@ __device__ __forceinline__ void warp_mma_rt(float (&acc)[NT][4], int kdim, FA a_
   }
 }
 
+// ---------------------------------------------------------------------------
+// split-tf32 warp MMA (m16n8k8): x = hi + lo with hi = tf32(x), lo = tf32(x - hi)
+// (about 21 mantissa bits); a product is lo*hi + hi*lo + hi*hi, accumulated in
+// fp32 on the tensor cores.  Operands come straight from registers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  uint32_t h, l;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
+  const float r = x - __uint_as_float(h);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(r));
+  hi = h;
+  lo = l;
+}
+
+__device__ __forceinline__ void mma1688_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// acc (a 16 x 8 fp32 tile, accumulator layout) += A B over k = k0 .. k0 + 7,
+// a_at(m, k) and b_at(k, n) giving fp32 elements relative to the tile origin
+template <typename FA, typename FB>
+__device__ __forceinline__ void warp_mma_tf32x3(float (&acc)[4], int k0, FA a_at, FB b_at) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+  uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+  split_tf32(a_at(gq, k0 + tq), ah[0], al[0]);
+  split_tf32(a_at(gq + 8, k0 + tq), ah[1], al[1]);
+  split_tf32(a_at(gq, k0 + tq + 4), ah[2], al[2]);
+  split_tf32(a_at(gq + 8, k0 + tq + 4), ah[3], al[3]);
+  split_tf32(b_at(k0 + tq, gq), bh0, bl0);
+  split_tf32(b_at(k0 + tq + 4, gq), bh1, bl1);
+  mma1688_tf32(acc, al, bh0, bh1);
+  mma1688_tf32(acc, ah, bl0, bl1);
+  mma1688_tf32(acc, ah, bh0, bh1);
+}
+
 // Row / column of accumulator element e of n-tile nt for this lane.
 __device__ __forceinline__ int acc_row(int e) { return ((threadIdx.x & 31) >> 2) + ((e & 2) ? 8 : 0); }
 __device__ __forceinline__ int acc_col(int nt, int e) { return nt * 8 + 2 * (threadIdx.x & 3) + (e & 1); }

@@ -10,18 +10,23 @@
 //   G  = [K; Q] K^T          M = 128 (keys then queries), N = C, K = dk
 // Each warpgroup then, for its value head (gates and beta differ per head):
 //   A    = strict-lower(beta_r G_rs exp(b_r - b_s)), Aqk = lower(scale P_rs
-//          exp(b_r - b_s)) straight from its tensor-memory lanes (pairwise
-//          decays only for s <= r: no exponent is positive)
-//   T    = (I + A)^-1 by the blocked solve of ROCm/rocm-libraries PR #11223
-//          ("Levers" 3): 16 x 16 diagonal blocks by forward substitution, block
-//          rows by split-bf16 tensor-core products against the solved blocks
+//          exp(b_r - b_s)) straight from its tensor-memory lanes; inside a
+//          32-row block the decay is one exp2 per entry, across blocks it is
+//          exp(b_r - b_o) exp(b_o - b_s) with o the block's first row (both
+//          factors <= 1 for non-positive gates: nothing overflows)
+//   T    = (I + A)^-1 blocked as in ROCm/rocm-libraries PR #11223 ("Levers"
+//          3): each 32 x 32 diagonal block by forward substitution in registers
+//          (one warp per block, one thread per column), then the off-diagonal
+//          block T10 = -T11 (A10 T00); fp32 on the CUDA cores throughout
 //   P1   = K^T (D T)         the key tile read MN-major, D = diag(exp(b_last - b_s))
 //   AqkT = Aqk T
 //   E    = K_next P1         (fp16 P1 as the B operand; zero for the last chunk
 //                             of a sequence)
 // and writes them, each rounded once to fp16, as the 32 KB operand image of the
 // lookahead scan kernel (rows 0..127 = P1, 128..191 = E, 192..255 = AqkT;
-// K-major, 128-byte swizzle) straight from registers.  E lets the scan form
+// K-major, 128-byte swizzle), staged in shared memory and stored with one bulk
+// copy.  The staged P1 rows double as E's B operand: a K-major image of P1's
+// dk rows is the MN-major layout of P1 read as a dk x C operand.  E lets the scan form
 // the next chunk's K S from this chunk's Y without waiting for the state:
 //   K_next S_next = exp(b_last) K_next S + E Y.
 #include <cuda.h>
@@ -48,18 +53,18 @@ __device__ __forceinline__ float ex2(float x) {
 
 template <int C, int NWG>
 struct PrepTmemSmem {
-  static constexpr int LDC = C + 1;               // fp32 row stride of A / T (odd)
+  static constexpr int LDT = C + 4;               // fp32 row stride of A^T / T^T
   // [K; Q; K_next], K-major, always two panels of 192 rows x 128 bytes
   static constexpr int PANEL = 192 * 128;
   static constexpr int KQ = 2 * PANEL;
   // per warpgroup
   static constexpr int WG_AQK = 0;                // Aqk, K-major, 64 rows (8 KB)
-  static constexpr int WG_P1 = 0;                 // later: P1, MN-major, dk K-rows (16 KB)
-  static constexpr int WG_TI = 8 * 1024;          // T, MN-major, 64 K-rows (8 KB)
-  static constexpr int WG_DTI = 16 * 1024;        // D T, MN-major (8 KB)
-  static constexpr int WG_A = 24 * 1024;          // A -> T, fp32
-  static constexpr int WG_R = WG_A + C * LDC * 4;  // 16 x LDC scratch
-  static constexpr int WG_G = WG_R + 16 * LDC * 4;  // cumulative gates (log2 units)
+  static constexpr int WG_IMG = 0;                // later: the 32 KB output image
+  static constexpr int WG_TI = 8 * 1024;          // T as a K-major B operand (8 KB)
+  static constexpr int WG_DTI = 16 * 1024;        // D T, likewise (8 KB)
+  static constexpr int WG_A = 24 * 1024;          // A^T -> T^T, fp32, row stride LDT
+  static constexpr int WG_R = WG_A + C * LDT * 4;  // 32 x 36 scratch (W tiles)
+  static constexpr int WG_G = WG_R + 32 * 36 * 4;  // cumulative gates (log2 units)
   static constexpr int WG_BETA = WG_G + C * 4;
   static constexpr int WG_DEC = WG_BETA + C * 4;
   static constexpr int WG_BYTES = ((WG_DEC + C * 4 + 1023) / 1024) * 1024;
@@ -75,7 +80,7 @@ template <int C, int DK, int NWG>
 __global__ void __launch_bounds__(128 * NWG, 1)
 gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   using SM = PrepTmemSmem<C, NWG>;
-  constexpr int LDC = SM::LDC;
+  constexpr int LDT = SM::LDT;
   constexpr int NT = 128 * NWG;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -88,9 +93,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   int *meta = reinterpret_cast<int *>(sm + SM::kMisc + 8);
 
   const int slot = blockIdx.x, hq = blockIdx.y;
-  const int G = a.HV / a.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int wg = warp >> 2, t = tid & 127;  // warpgroup, thread within it
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
   // ---- slot -> (sequence, chunk) ----
@@ -139,6 +142,18 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       if (Ln > 0) tma_load_3d(smem_addr(kq + p * SM::PANEL + 128 * 128), &maps.k, p * 64, hq, t0 + C, bar_tma);
     }
   }
+  // this warpgroup's first gates and beta, fetched while the tiles land
+  const int wg = warp >> 2, t = tid & 127;  // warpgroup, thread within it
+  const int G = a.HV / a.H;
+  float g_next = 0.f, b_next = 0.f;
+  auto fetch = [&](int j) {
+    if (t < C && t < L && j < G) {
+      const long row = (long)(t0 + t) * a.HV + hq * G + j;
+      g_next = __ldg(a.g + row);
+      b_next = __ldg(a.beta + row);
+    }
+  };
+  fetch(wg);
   mbar_wait(bar_tma, 0, abort_flag);
   // bf16 -> fp16 in place; rows beyond each tile's tokens -> 0
   {
@@ -177,15 +192,16 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     }
     mma_commit(bar_gram);
   }
-  // publish [K_next; Q] (rows 128.. and 64.. of each panel) while the Gram runs
-  {
-    constexpr int KQB = kq_image_bytes(DK);
-    uint4 *dst = reinterpret_cast<uint4 *>(a.kq_images + ((size_t)slot * a.H + hq) * KQB);
-    for (int i = tid; i < KQB / 16; i += NT) {
-      const int p = i >> 10, within = (i & 1023) * 16;  // 16 KB per image panel
-      const int from = p * SM::PANEL + (within < 8192 ? 16384 + within : within);
-      dst[i] = *reinterpret_cast<const uint4 *>(kq + from);
+  // publish [K_next; Q] (rows 128.. and 64.. of each panel) while the Gram
+  // runs: bulk stores, completed before the CTA ends
+  if (tid == 0) {
+    unsigned char *dst = a.kq_images + ((size_t)slot * a.H + hq) * kq_image_bytes(DK);
+#pragma unroll
+    for (int p = 0; p < DK / 64; p++) {
+      bulk_s2g(dst + p * 16384, smem_addr(kq + p * SM::PANEL + 16384), 8192);
+      bulk_s2g(dst + p * 16384 + 8192, smem_addr(kq + p * SM::PANEL + 8192), 8192);
     }
+    bulk_commit();
   }
 
   // ---- per value head, one warpgroup each ----
@@ -200,15 +216,19 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   const int wlane0 = (warp & 3) * 32;  // first tensor-memory lane of this warp
   int mma_uses = 0;  // completions of bar_mma so far
   bool first = true;
+  float *Wf = Rs;  // exp2(b_32 - b_s), s < 32 (the cross-block decay factors)
   for (int j = wg; j < G; j += NWG) {
     const int hv = hq * G + j;
     // gates (log2 units), beta, cumulative gates, end-of-chunk decays
+    const float gv = g_next, bv = b_next;
+    g_next = 0.f;
+    b_next = 0.f;
+    fetch(j + NWG);
     bool positive = false;
     if (t < C) {
-      const float gv = t < L ? __ldg(a.g + (long)(t0 + t) * a.HV + hv) : 0.f;
       positive = gv > 0.f;
       Gs[t] = gv * kLog2e;
-      Bs[t] = t < L ? __ldg(a.beta + (long)(t0 + t) * a.HV + hv) : 0.f;
+      Bs[t] = bv;
     }
     if (__any_sync(0xffffffffu, positive) && lane == 0) atomicOr(a.flags, kFlagPositiveGate);
     named_bar(1 + wg, 128);
@@ -225,6 +245,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       const float blast = __shfl_sync(0xffffffffu, C > 32 ? x1 : x0, (C - 1) & 31);
       if (lane < C) { Gs[lane] = x0; Ds[lane] = ex2(blast - x0); }
       if (lane + 32 < C) { Gs[lane + 32] = x1; Ds[lane + 32] = ex2(blast - x1); }
+      if (C > 32) Wf[lane] = ex2(__shfl_sync(0xffffffffu, x1, 0) - x0);
     }
     named_bar(1 + wg, 128);
     if (first) {
@@ -234,29 +255,47 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     }
 
     // ---- A (key lanes) and Aqk (query lanes) from the shared Gram ----
+    // decay of column s for row r in 32-row block o: direct inside the block,
+    // factored (ur * Wf[s]) for the earlier block.  A is stored transposed
+    // (As[s * LDT + r] = A[r][s]): the solve reads its columns as rows.
     if (wlane0 < C) {
-      const int r = t;
+      const int r = t, o = wlane0;
       const float br = Gs[r], beta = Bs[r];
+      const float bu = o > 0 ? beta * ex2(br - Gs[o]) : 0.f;
 #pragma unroll
       for (int h = 0; h < C / 32; h++) {
+        if (32 * h > o) {  // s > r throughout
+#pragma unroll
+          for (int i = 0; i < 32; i++) As[(32 * h + i) * LDT + r] = 0.f;
+          continue;
+        }
         uint32_t g[32];
         tmem_ld32_nowait(tmem + lane_base + 32 * h, g);
         tmem_wait_ld();
+        if (32 * h < o) {
 #pragma unroll
-        for (int i = 0; i < 32; i++) {
-          const int s = 32 * h + i;
-          As[r * LDC + s] = s < r ? beta * __uint_as_float(g[i]) * ex2(br - Gs[s]) : 0.f;
+          for (int i = 0; i < 32; i++) As[(32 * h + i) * LDT + r] = bu * __uint_as_float(g[i]) * Wf[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i++) {
+            const int s = 32 * h + i;
+            As[s * LDT + r] = s < r ? beta * __uint_as_float(g[i]) * ex2(br - Gs[s]) : 0.f;
+          }
         }
       }
     } else if (wlane0 >= 64 && wlane0 - 64 < C) {
-      const int r = t - 64;
+      const int r = t - 64, o = wlane0 - 64;
       const float br = Gs[r];
+      const float su = o > 0 ? a.scale * ex2(br - Gs[o]) : 0.f;
       unsigned char *aq = ws + SM::WG_AQK;
 #pragma unroll
       for (int h = 0; h < C / 32; h++) {
         uint32_t g[32];
-        tmem_ld32_nowait(tmem + lane_base + 32 * h, g);
-        tmem_wait_ld();
+        const bool any = 32 * h <= o;
+        if (any) {
+          tmem_ld32_nowait(tmem + lane_base + 32 * h, g);
+          tmem_wait_ld();
+        }
 #pragma unroll
         for (int ch = 0; ch < 4; ch++) {
           uint4 pk;
@@ -264,8 +303,14 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
 #pragma unroll
           for (int i = 0; i < 4; i++) {
             const int s = 32 * h + ch * 8 + 2 * i;
-            const float v0 = s <= r ? a.scale * __uint_as_float(g[ch * 8 + 2 * i]) * ex2(br - Gs[s]) : 0.f;
-            const float v1 = s + 1 <= r ? a.scale * __uint_as_float(g[ch * 8 + 2 * i + 1]) * ex2(br - Gs[s + 1]) : 0.f;
+            float v0 = 0.f, v1 = 0.f;
+            if (32 * h < o) {
+              v0 = su * __uint_as_float(g[ch * 8 + 2 * i]) * Wf[s];
+              v1 = su * __uint_as_float(g[ch * 8 + 2 * i + 1]) * Wf[s + 1];
+            } else if (any) {
+              v0 = s <= r ? a.scale * __uint_as_float(g[ch * 8 + 2 * i]) * ex2(br - Gs[s]) : 0.f;
+              v1 = s + 1 <= r ? a.scale * __uint_as_float(g[ch * 8 + 2 * i + 1]) * ex2(br - Gs[s + 1]) : 0.f;
+            }
             ph[i] = __floats2half2_rn(v0, v1);
           }
           *reinterpret_cast<uint4 *>(aq + kmajor_off(r, 32 * h + ch * 8, 64)) = pk;
@@ -275,71 +320,117 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     fence_before_sync();
     named_bar(1 + wg, 128);
 
-    // ---- T = (I + A)^-1, in place ----
-    constexpr int NB = C / 16;
+    // ---- T = (I + A)^-1, transposed in place: As[j * LDT + r] = T[r][j] ----
+    // (1) 16 x 16 diagonal blocks: warp w, lanes 0..15 = columns, rows in
+    //     registers, forward substitution in fp32
     {
-      float x[16];
-      const int I = t / 16, jj = t % 16, o = 16 * I;
-      if (t < NB * 16) {
+      const int wq = warp & 3;
+      if (wq < C / 16 && lane < 16) {
+        const int o = 16 * wq;
+        float x[16];
 #pragma unroll
-        for (int r = 0; r < 16; r++) x[r] = (r == jj) ? 1.f : 0.f;
+        for (int r = 0; r < 16; r++) x[r] = r == lane ? 1.f : 0.f;
 #pragma unroll
-        for (int s = 0; s < 16; s++) {
-          const float xs = x[s];
+        for (int s2 = 0; s2 < 15; s2++) {
+          const float xs = x[s2];
+          const float *col = As + (o + s2) * LDT + o;  // A[o + r][o + s2], r = 0..15
 #pragma unroll
-          for (int r = s + 1; r < 16; r++) x[r] -= As[(o + r) * LDC + o + s] * xs;
+          for (int m = (s2 + 1) / 4; m < 4; m++) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(col + 4 * m);
+            if (4 * m + 0 > s2) x[4 * m + 0] = fmaf(-a4.x, xs, x[4 * m + 0]);
+            if (4 * m + 1 > s2) x[4 * m + 1] = fmaf(-a4.y, xs, x[4 * m + 1]);
+            if (4 * m + 2 > s2) x[4 * m + 2] = fmaf(-a4.z, xs, x[4 * m + 2]);
+            if (4 * m + 3 > s2) x[4 * m + 3] = fmaf(-a4.w, xs, x[4 * m + 3]);
+          }
         }
+        __syncwarp(0x0000ffffu);
+        float *row = As + (o + lane) * LDT + o;  // T[o + r][o + lane]
+#pragma unroll
+        for (int m = 0; m < 4; m++)
+          *reinterpret_cast<float4 *>(row + 4 * m) = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
       }
       named_bar(1 + wg, 128);
-      if (t < NB * 16) {
-#pragma unroll
-        for (int r = 0; r < 16; r++) As[(o + r) * LDC + o + jj] = x[r];
+      // (2) 32 x 32 blocks from their 16 x 16 halves: T10 = -T11 (A10 T00),
+      //     one warp per (32-block, 8-column tile); split-tf32 tensor-core
+      //     products (fp32-class accuracy), W staged in the warp's rows of Rs
+      const int gq = lane >> 2, tq = lane & 3;
+      const bool act2 = wq < 2 * (C / 32);
+      const int ob = 32 * (wq >> 1), n2 = 8 * (wq & 1);
+      float *Wt2 = Rs + wq * 16 * 9;  // this warp's 16 x 8 W tile, row stride 9
+      if (act2) {
+        float w[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k0 = 0; k0 < 16; k0 += 8)
+          warp_mma_tf32x3(w, k0, [&](int m, int k) { return As[(ob + k) * LDT + ob + 16 + m]; },
+                          [&](int k, int n) { return As[(ob + n2 + n) * LDT + ob + k]; });
+        Wt2[gq * 9 + 2 * tq] = w[0]; Wt2[gq * 9 + 2 * tq + 1] = w[1];
+        Wt2[(gq + 8) * 9 + 2 * tq] = w[2]; Wt2[(gq + 8) * 9 + 2 * tq + 1] = w[3];
+      }
+      named_bar(1 + wg, 128);  // both warps of a block have read A10 before T10 overwrites it
+      if (act2) {
+        float u[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k0 = 0; k0 < 16; k0 += 8)
+          warp_mma_tf32x3(u, k0, [&](int m, int k) { return As[(ob + 16 + k) * LDT + ob + 16 + m]; },
+                          [&](int k, int n) { return Wt2[k * 9 + n]; });
+        // T10[r][c] -> As[(ob + n2 + c) LDT + ob + 16 + r], over A10^T
+        As[(ob + n2 + 2 * tq) * LDT + ob + 16 + gq] = -u[0];
+        As[(ob + n2 + 2 * tq + 1) * LDT + ob + 16 + gq] = -u[1];
+        As[(ob + n2 + 2 * tq) * LDT + ob + 24 + gq] = -u[2];
+        As[(ob + n2 + 2 * tq + 1) * LDT + ob + 24 + gq] = -u[3];
       }
       named_bar(1 + wg, 128);
-    }
-    for (int I = 1; I < NB; I++) {
-      const int w = 16 * I, J = warp & 3;
-      if (J < I) {
-        float acc[2][4] = {};
-        warp_mma_rt<2, false, false>(
-            acc, w - 16 * J, [&](int m, int k) { return As[(w + m) * LDC + 16 * J + k]; },
-            [&](int k, int n) { return As[(16 * J + k) * LDC + 16 * J + n]; });
+      if constexpr (C == 64) {
+        // (3) the 64 x 64 inverse from its 32 x 32 halves: T10 = -T11 (A10 T00),
+        //     warp w owns columns 8w .. 8w+7 of W and of T10
+        const int n0 = 8 * wq;
+        float w[2][4] = {};
 #pragma unroll
-        for (int nt = 0; nt < 2; nt++)
+        for (int mt = 0; mt < 2; mt++)
+          for (int k0 = 0; k0 < 32; k0 += 8)
+            warp_mma_tf32x3(w[mt], k0, [&](int m, int k) { return As[k * LDT + 32 + 16 * mt + m]; },
+                            [&](int k, int n) { return As[(n0 + n) * LDT + k]; });
+        float *Wt = Rs + wq * 32 * 9;  // this warp's 32 x 8 W tile, row stride 9
 #pragma unroll
-          for (int e = 0; e < 4; e++) Rs[acc_row(e) * LDC + 16 * J + acc_col(nt, e)] = acc[nt][e];
+        for (int mt = 0; mt < 2; mt++) {
+          Wt[(16 * mt + gq) * 9 + 2 * tq] = w[mt][0]; Wt[(16 * mt + gq) * 9 + 2 * tq + 1] = w[mt][1];
+          Wt[(16 * mt + gq + 8) * 9 + 2 * tq] = w[mt][2]; Wt[(16 * mt + gq + 8) * 9 + 2 * tq + 1] = w[mt][3];
+        }
+        named_bar(1 + wg, 128);  // every warp has read A10 before T10 overwrites it
+        float u[2][4] = {};
+#pragma unroll
+        for (int mt = 0; mt < 2; mt++)
+          for (int k0 = 0; k0 < 16 * (mt + 1); k0 += 8)  // T11 lower triangular
+            warp_mma_tf32x3(u[mt], k0, [&](int m, int k) { return As[(32 + k) * LDT + 32 + 16 * mt + m]; },
+                            [&](int k, int n) { return Wt[k * 9 + n]; });
+#pragma unroll
+        for (int mt = 0; mt < 2; mt++) {
+          As[(n0 + 2 * tq) * LDT + 32 + 16 * mt + gq] = -u[mt][0];
+          As[(n0 + 2 * tq + 1) * LDT + 32 + 16 * mt + gq] = -u[mt][1];
+          As[(n0 + 2 * tq) * LDT + 40 + 16 * mt + gq] = -u[mt][2];
+          As[(n0 + 2 * tq + 1) * LDT + 40 + 16 * mt + gq] = -u[mt][3];
+        }
+        named_bar(1 + wg, 128);
       }
-      named_bar(1 + wg, 128);
-      if (J < I) {
-        float acc[2][4] = {};
-        warp_mma<16, 2, false, false>(
-            acc, [&](int m, int k) { return As[(w + m) * LDC + w + k]; },
-            [&](int k, int n) { return Rs[k * LDC + 16 * J + n]; });
-#pragma unroll
-        for (int nt = 0; nt < 2; nt++)
-#pragma unroll
-          for (int e = 0; e < 4; e++) As[(w + acc_row(e)) * LDC + 16 * J + acc_col(nt, e)] = -acc[nt][e];
-      }
-      named_bar(1 + wg, 128);
     }
 
-    // ---- fp16 images of T and D T (MN-major: K-row s holds T[s][0..C)) ----
+    // ---- fp16 images of T and D T as K-major B operands: row j = T[.][j] ----
     if (t < C) {
-      const int s = t;
-      const float d = Ds[s];
+      const int j = t;
+      const float *trow = As + j * LDT;
 #pragma unroll
       for (int ch = 0; ch < C / 8; ch++) {
+        const float4 t0v = *reinterpret_cast<const float4 *>(trow + ch * 8);
+        const float4 t1v = *reinterpret_cast<const float4 *>(trow + ch * 8 + 4);
+        const float4 d0 = *reinterpret_cast<const float4 *>(Ds + ch * 8);
+        const float4 d1 = *reinterpret_cast<const float4 *>(Ds + ch * 8 + 4);
         uint4 pt, pd;
         __half2 *ht = reinterpret_cast<__half2 *>(&pt);
         __half2 *hd = reinterpret_cast<__half2 *>(&pd);
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-          const float v0 = As[s * LDC + ch * 8 + 2 * i], v1 = As[s * LDC + ch * 8 + 2 * i + 1];
-          ht[i] = __floats2half2_rn(v0, v1);
-          hd[i] = __floats2half2_rn(d * v0, d * v1);
-        }
-        *reinterpret_cast<uint4 *>(ws + SM::WG_TI + mnmajor_chunk_off(s, ch, 64)) = pt;
-        *reinterpret_cast<uint4 *>(ws + SM::WG_DTI + mnmajor_chunk_off(s, ch, 64)) = pd;
+        ht[0] = __floats2half2_rn(t0v.x, t0v.y); ht[1] = __floats2half2_rn(t0v.z, t0v.w);
+        ht[2] = __floats2half2_rn(t1v.x, t1v.y); ht[3] = __floats2half2_rn(t1v.z, t1v.w);
+        hd[0] = __floats2half2_rn(d0.x * t0v.x, d0.y * t0v.y); hd[1] = __floats2half2_rn(d0.z * t0v.z, d0.w * t0v.w);
+        hd[2] = __floats2half2_rn(d1.x * t1v.x, d1.y * t1v.y); hd[3] = __floats2half2_rn(d1.z * t1v.z, d1.w * t1v.w);
+        *reinterpret_cast<uint4 *>(ws + SM::WG_TI + kmajor_off(j, ch * 8, 64)) = pt;
+        *reinterpret_cast<uint4 *>(ws + SM::WG_DTI + kmajor_off(j, ch * 8, 64)) = pd;
       }
     }
     fence_proxy_async();
@@ -351,30 +442,27 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     if (t == 0) {
       const uint32_t sKQ = smem_addr(kq), sAqk = smem_addr(ws + SM::WG_AQK);
       const uint32_t sT = smem_addr(ws + SM::WG_TI), sDT = smem_addr(ws + SM::WG_DTI);
-      constexpr uint32_t idP = idesc_f16(128, C, 1, 1);  // A MN-major: keys read as K^T
-      constexpr uint32_t idQ = idesc_f16(128, C, 0, 1);
+      constexpr uint32_t idP = idesc_f16(128, C, 1, 0);  // A MN-major: keys read as K^T
+      constexpr uint32_t idQ = idesc_f16(128, C, 0, 0);
 #pragma unroll
       for (int k0 = 0; k0 < C; k0 += 16) {
         mma_f16(tP1, make_desc(sKQ + k0 * 128, SM::PANEL, 1024),
-                make_desc(sDT + (k0 >> 4) * 2048, 8192, 1024), idP, k0 > 0 ? 1u : 0u);
+                make_desc(sDT + k0 * 2, 16, 1024), idP, k0 > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int k0 = 0; k0 < C; k0 += 16) {
         mma_f16(tAT, make_desc(sAqk + k0 * 2, 16, 1024),
-                make_desc(sT + (k0 >> 4) * 2048, 8192, 1024), idQ, k0 > 0 ? 1u : 0u);
+                make_desc(sT + k0 * 2, 16, 1024), idQ, k0 > 0 ? 1u : 0u);
       }
       mma_commit(bar_mma);
     }
     mbar_wait(bar_mma, mma_uses++ & 1, abort_flag);
     fence_after_sync();
 
-    // ---- the image, straight to HBM from the tensor-memory lanes ----
-    unsigned char *img = reinterpret_cast<unsigned char *>(a.tiles) +
-                         ((size_t)slot * a.HV + hv) * kLaImageBytes;
-    // image row `row` <- this lane's row at `taddr` (zeros when !have); with
-    // `mn`, the fp16 row also goes to shared memory as K-row t of an MN-major
-    // image (the B operand of E)
-    auto put_row = [&](int row, uint32_t taddr, bool have, unsigned char *mn) {
+    // ---- the image, staged in shared memory over the dead per-head buffers ----
+    unsigned char *img = ws + SM::WG_IMG;
+    // image row `row` <- this lane's row at `taddr` (zeros when !have)
+    auto put_row = [&](int row, uint32_t taddr, bool have) {
 #pragma unroll
       for (int h = 0; h < 2; h++) {  // 32 columns at a time
         uint32_t v[32];
@@ -394,12 +482,11 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
             hh[i] = __floats2half2_rn(f0, f1);
           }
           *reinterpret_cast<uint4 *>(img + kmajor_off(row, 32 * h + ch * 8, kLaImageRows)) = pk;
-          if (mn && 32 * h < C) *reinterpret_cast<uint4 *>(mn + mnmajor_chunk_off(t, 4 * h + ch, DK)) = pk;
         }
       }
     };
-    if (t < 64) put_row(192 + t, tAT + lane_base, wlane0 < C, nullptr);
-    put_row(t, tP1 + lane_base, wlane0 < DK, t < DK ? ws + SM::WG_P1 : nullptr);
+    if (t < 64) put_row(192 + t, tAT + lane_base, wlane0 < C);
+    put_row(t, tP1 + lane_base, wlane0 < DK);
     fence_proxy_async();
     fence_before_sync();
     named_bar(1 + wg, 128);
@@ -409,7 +496,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     //      into the Aqk T columns that were just read out ----
     if (Ln > 0) {
       if (t == 0) {
-        const uint32_t sKn = smem_addr(kq) + 128 * 128, sP1 = smem_addr(ws + SM::WG_P1);
+        const uint32_t sKn = smem_addr(kq) + 128 * 128, sP1 = smem_addr(img);
         constexpr uint32_t idE = idesc_f16(128, C, 0, 1);
 #pragma unroll
         for (int k0 = 0; k0 < DK; k0 += 16) {
@@ -421,10 +508,19 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       mbar_wait(bar_mma, mma_uses++ & 1, abort_flag);
       fence_after_sync();
     }
-    if (t < 64) put_row(128 + t, tAT + lane_base, Ln > 0 && wlane0 < C, nullptr);
+    if (t < 64) put_row(128 + t, tAT + lane_base, Ln > 0 && wlane0 < C);
+    fence_proxy_async();
     fence_before_sync();
     named_bar(1 + wg, 128);
+    if (t == 0) {
+      bulk_s2g(reinterpret_cast<unsigned char *>(a.tiles) + ((size_t)slot * a.HV + hv) * kLaImageBytes,
+               smem_addr(img), kLaImageBytes);
+      bulk_commit();
+      bulk_wait_read_all();  // the staging area is reused by the next head
+    }
+    named_bar(1 + wg, 128);
   }
+  if (t == 0) bulk_wait_all();
 
   // ---- tear-down ----
   fence_before_sync();

@@ -169,6 +169,24 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_saddr, const void *src, ui
       : "memory");
 }
 
+// bulk copy shared -> global, in the issuing thread's bulk async-group
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_saddr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(src_saddr), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the issuing thread's bulk stores have read their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// the issuing thread's bulk stores have completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // TMA: 3-D tiled load of box {x, y, z} at coordinates (x, y, z) of `tmap`
 // (a __grid_constant__ CUtensorMap), completing transactions on `bar`
 __device__ __forceinline__ void tma_load_3d(uint32_t dst_saddr, const void *tmap, int x, int y,
