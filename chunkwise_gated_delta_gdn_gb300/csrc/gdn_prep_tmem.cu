@@ -83,8 +83,9 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   constexpr int LDT = SM::LDT;
   constexpr int NT = 128 * NWG;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1 KB-aligned base, as an offset into the shared array (the compiler then
+  // knows every access below is to shared memory)
+  unsigned char *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
   unsigned char *kq = sm + SM::kKQ;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::kBar);
   const uint32_t bar_tma = smem_addr(bars), bar_gram = smem_addr(bars + 1);

@@ -110,8 +110,9 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   using SM = LaSmem<C, DK>;
   constexpr int NKQ = SM::NKQ, NP = SM::NP, NCF = SM::NCF;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1 KB-aligned base, as an offset into the shared array (the compiler then
+  // knows every access below is to shared memory)
+  unsigned char *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (sm - smem_raw > SM::kSlack) {  // dynamic shared memory not aligned as needed
     if (tid == 0) atomicOr(a.flags, kFlagTimeout);

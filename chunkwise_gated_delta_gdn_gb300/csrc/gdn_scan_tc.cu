@@ -86,8 +86,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   using SM = ScanTcSmem<C, DK, GATE, NST>;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1 KB-aligned base, as an offset into the shared array (the compiler then
+  // knows every access below is to shared memory)
+  unsigned char *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (sm - smem_raw > SM::kSlack) {  // dynamic shared memory not aligned as needed
     if (tid == 0) atomicOr(a.flags, kFlagTimeout);
