@@ -1,8 +1,10 @@
 // gdn_prep_tmem.cu -- chunk-prep kernel of the bf16 scalar-gate (GDN) path on
 // the 5th-generation tensor cores.
 //
-// One CTA per (chunk slot, q/k head), one warpgroup (128 threads) per value
-// head of the group (up to three at once).  The group shares the key/query
+// One CTA per (chunk slot, q/k head); its warpgroup (128 threads) takes the
+// group's value heads in turn (the kernel is written for NWG warpgroups taking
+// them in parallel; one measured faster, two CTAs sharing an SM).  The group
+// shares the key/query
 // tile and the next chunk's key tile: they arrive once by TMA (bf16, 128-byte
 // swizzle), are converted to fp16 in place, published for the scan kernel as
 // its [K_next; Q] operand image, and feed one Gram product for all value
@@ -77,7 +79,7 @@ struct PrepTmemSmem {
 };
 
 template <int C, int DK, int NWG>
-__global__ void __launch_bounds__(128 * NWG, 1)
+__global__ void __launch_bounds__(128 * NWG, NWG == 1 ? 2 : 1)
 gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   using SM = PrepTmemSmem<C, NWG>;
   constexpr int LDT = SM::LDT;
@@ -126,7 +128,9 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   if (!meta[2]) return;  // unused slot: the scan never reads it
   const int t0 = meta[0], L = meta[1], Ln = meta[3];
 
-  if (warp == 0) tmem_alloc(smem_addr(tslot), 512);
+  // Gram (C columns) + per warpgroup P1 and Aqk T / E (2 x 64)
+  constexpr uint32_t kCols = NWG == 1 ? 256 : 512;
+  if (warp == 0) tmem_alloc(smem_addr(tslot), kCols);
   if (C < 64) {  // zero the rows no TMA box covers
     for (int i = tid; i < SM::KQ / 16; i += NT) {
       const int row = (i * 16 % SM::PANEL) / 128;
@@ -527,7 +531,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 0) tmem_dealloc(tmem, 512);
+  if (warp == 0) tmem_dealloc(tmem, kCols);
   if (*abort_flag && tid == 0) atomicOr(a.flags, kFlagTimeout);
 }
 
@@ -544,9 +548,10 @@ cudaError_t launch_one(const PrepArgs &a, const ScanMaps &maps, cudaStream_t str
 
 template <int C, int DK>
 cudaError_t dispatch_wg(const PrepArgs &a, const ScanMaps &maps, cudaStream_t s) {
-  const int G = a.HV / a.H;
-  if (G % 3 == 0) return launch_one<C, DK, 3>(a, maps, s);
-  if (G % 2 == 0) return launch_one<C, DK, 2>(a, maps, s);
+  // one warpgroup walking the group's value heads in turn: about 97 KB of
+  // shared memory and 256 tensor-memory columns, so two CTAs share an SM and
+  // overlap each other's latency-bound phases (measured faster than one
+  // warpgroup per value head at one CTA per SM)
   return launch_one<C, DK, 1>(a, maps, s);
 }
 
