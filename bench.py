@@ -342,7 +342,7 @@ def main():
     achieved = kbytes / (kern_ms / 1e3) / 1e9
     traffic, traffic_note = measured_traffic(c0.name, dominant, c0.tokens)
     kernel_names = {  # kernels gdn_chunk_fwd launches for this workload
-        ("prep", "bf16", 0): "gdn_prep_tmem_kernel", ("scan", "bf16", 0): "gdn_scan_tc_kernel",
+        ("prep", "bf16", 0): "gdn_prep_tmem_kernel", ("scan", "bf16", 0): "gdn_scan_la_kernel",
         ("prep", "bf16", 1): "gdn_prep_tc_kernel", ("scan", "bf16", 1): "gdn_scan_tc_kernel",
         ("prep", "f32", 0): "gdn_prep_kernel", ("scan", "f32", 0): "gdn_scan_kernel",
         ("prep", "f32", 1): "gdn_prep_kernel", ("scan", "f32", 1): "gdn_scan_kernel"}
