@@ -189,9 +189,13 @@ __device__ __forceinline__ void mma1688_tf32(float (&c)[4], const uint32_t (&a)[
 }
 
 // acc (a 16 x 8 fp32 tile, accumulator layout) += A B over k = k0 .. k0 + 7,
-// a_at(m, k) and b_at(k, n) giving fp32 elements relative to the tile origin
+// a_at(m, k) and b_at(k, n) giving fp32 elements relative to the tile origin.
+// The hi*hi terms go to `acc`, the two correction terms to `corr` (added to
+// acc by the caller at the end), so the three products of a step do not wait
+// on one another.
 template <typename FA, typename FB>
-__device__ __forceinline__ void warp_mma_tf32x3(float (&acc)[4], int k0, FA a_at, FB b_at) {
+__device__ __forceinline__ void warp_mma_tf32x3(float (&acc)[4], float (&corr)[4], int k0,
+                                                FA a_at, FB b_at) {
   const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
   uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
   split_tf32(a_at(gq, k0 + tq), ah[0], al[0]);
@@ -200,9 +204,9 @@ __device__ __forceinline__ void warp_mma_tf32x3(float (&acc)[4], int k0, FA a_at
   split_tf32(a_at(gq + 8, k0 + tq + 4), ah[3], al[3]);
   split_tf32(b_at(k0 + tq, gq), bh0, bl0);
   split_tf32(b_at(k0 + tq + 4, gq), bh1, bl1);
-  mma1688_tf32(acc, al, bh0, bh1);
-  mma1688_tf32(acc, ah, bl0, bl1);
   mma1688_tf32(acc, ah, bh0, bh1);
+  mma1688_tf32(corr, al, bh0, bh1);
+  mma1688_tf32(corr, ah, bl0, bl1);
 }
 
 // Row / column of accumulator element e of n-tile nt for this lane.

@@ -259,6 +259,12 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       first = false;
     }
 
+    // the previous head's image store must have read the staging area, which
+    // the writes below reuse
+    if (j != wg) {
+      if (t == 0) bulk_wait_read_all();
+      named_bar(1 + wg, 128);
+    }
     // ---- A (key lanes) and Aqk (query lanes) from the shared Gram ----
     // decay of column s for row r in 32-row block o: direct inside the block,
     // factored (ur * Wf[s]) for the earlier block.  A is stored transposed
@@ -363,19 +369,25 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       const int ob = 32 * (wq >> 1), n2 = 8 * (wq & 1);
       float *Wt2 = Rs + wq * 16 * 9;  // this warp's 16 x 8 W tile, row stride 9
       if (act2) {
-        float w[4] = {0.f, 0.f, 0.f, 0.f};
+        float w[4] = {0.f, 0.f, 0.f, 0.f}, wc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
         for (int k0 = 0; k0 < 16; k0 += 8)
-          warp_mma_tf32x3(w, k0, [&](int m, int k) { return As[(ob + k) * LDT + ob + 16 + m]; },
+          warp_mma_tf32x3(w, wc, k0, [&](int m, int k) { return As[(ob + k) * LDT + ob + 16 + m]; },
                           [&](int k, int n) { return As[(ob + n2 + n) * LDT + ob + k]; });
+#pragma unroll
+        for (int e = 0; e < 4; e++) w[e] += wc[e];
         Wt2[gq * 9 + 2 * tq] = w[0]; Wt2[gq * 9 + 2 * tq + 1] = w[1];
         Wt2[(gq + 8) * 9 + 2 * tq] = w[2]; Wt2[(gq + 8) * 9 + 2 * tq + 1] = w[3];
       }
       named_bar(1 + wg, 128);  // both warps of a block have read A10 before T10 overwrites it
       if (act2) {
-        float u[4] = {0.f, 0.f, 0.f, 0.f};
+        float u[4] = {0.f, 0.f, 0.f, 0.f}, uc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
         for (int k0 = 0; k0 < 16; k0 += 8)
-          warp_mma_tf32x3(u, k0, [&](int m, int k) { return As[(ob + 16 + k) * LDT + ob + 16 + m]; },
+          warp_mma_tf32x3(u, uc, k0, [&](int m, int k) { return As[(ob + 16 + k) * LDT + ob + 16 + m]; },
                           [&](int k, int n) { return Wt2[k * 9 + n]; });
+#pragma unroll
+        for (int e = 0; e < 4; e++) u[e] += uc[e];
         // T10[r][c] -> As[(ob + n2 + c) LDT + ob + 16 + r], over A10^T
         As[(ob + n2 + 2 * tq) * LDT + ob + 16 + gq] = -u[0];
         As[(ob + n2 + 2 * tq + 1) * LDT + ob + 16 + gq] = -u[1];
@@ -387,12 +399,17 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
         // (3) the 64 x 64 inverse from its 32 x 32 halves: T10 = -T11 (A10 T00),
         //     warp w owns columns 8w .. 8w+7 of W and of T10
         const int n0 = 8 * wq;
-        float w[2][4] = {};
+        float w[2][4] = {}, wc[2][4] = {};
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 8)
+#pragma unroll
+          for (int mt = 0; mt < 2; mt++)
+            warp_mma_tf32x3(w[mt], wc[mt], k0, [&](int m, int k) { return As[k * LDT + 32 + 16 * mt + m]; },
+                            [&](int k, int n) { return As[(n0 + n) * LDT + k]; });
 #pragma unroll
         for (int mt = 0; mt < 2; mt++)
-          for (int k0 = 0; k0 < 32; k0 += 8)
-            warp_mma_tf32x3(w[mt], k0, [&](int m, int k) { return As[k * LDT + 32 + 16 * mt + m]; },
-                            [&](int k, int n) { return As[(n0 + n) * LDT + k]; });
+#pragma unroll
+          for (int e = 0; e < 4; e++) w[mt][e] += wc[mt][e];
         float *Wt = Rs + wq * 32 * 9;  // this warp's 32 x 8 W tile, row stride 9
 #pragma unroll
         for (int mt = 0; mt < 2; mt++) {
@@ -400,12 +417,18 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
           Wt[(16 * mt + gq + 8) * 9 + 2 * tq] = w[mt][2]; Wt[(16 * mt + gq + 8) * 9 + 2 * tq + 1] = w[mt][3];
         }
         named_bar(1 + wg, 128);  // every warp has read A10 before T10 overwrites it
-        float u[2][4] = {};
+        float u[2][4] = {}, uc[2][4] = {};
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 8)
+#pragma unroll
+          for (int mt = 0; mt < 2; mt++)
+            if (k0 < 16 * (mt + 1))  // T11 lower triangular
+              warp_mma_tf32x3(u[mt], uc[mt], k0, [&](int m, int k) { return As[(32 + k) * LDT + 32 + 16 * mt + m]; },
+                              [&](int k, int n) { return Wt[k * 9 + n]; });
 #pragma unroll
         for (int mt = 0; mt < 2; mt++)
-          for (int k0 = 0; k0 < 16 * (mt + 1); k0 += 8)  // T11 lower triangular
-            warp_mma_tf32x3(u[mt], k0, [&](int m, int k) { return As[(32 + k) * LDT + 32 + 16 * mt + m]; },
-                            [&](int k, int n) { return Wt[k * 9 + n]; });
+#pragma unroll
+          for (int e = 0; e < 4; e++) u[mt][e] += uc[mt][e];
 #pragma unroll
         for (int mt = 0; mt < 2; mt++) {
           As[(n0 + 2 * tq) * LDT + 32 + 16 * mt + gq] = -u[mt][0];
@@ -521,7 +544,6 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       bulk_s2g(reinterpret_cast<unsigned char *>(a.tiles) + ((size_t)slot * a.HV + hv) * kLaImageBytes,
                smem_addr(img), kLaImageBytes);
       bulk_commit();
-      bulk_wait_read_all();  // the staging area is reused by the next head
     }
     named_bar(1 + wg, 128);
   }
