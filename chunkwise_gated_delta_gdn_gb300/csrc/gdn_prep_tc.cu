@@ -52,7 +52,11 @@ struct PrepTcSmem {
   static constexpr int kG = kR + 16 * LDC * 4;                 // gates -> b -> Kt (KDA)
   static constexpr int kBeta = kG + C * LDG * 4;
   static constexpr int kMeta = kBeta + C * 4;
-  static constexpr int kBytes = kMeta + 16;
+  // per-key gate: factored operands of one 16-row block (K~, Q~, then K^ for
+  // up to C rows), fp32, row stride LDX
+  static constexpr int LDX = DK + 4;
+  static constexpr int kX = (kMeta + 16 + 15) / 16 * 16;
+  static constexpr int kBytes = GATE == 0 ? kMeta + 16 : kX + (32 + C) * LDX * 4;
   static_assert(kImgSpan >= kPrepImageBytes, "image must fit the Q + A regions");
 };
 
@@ -127,37 +131,43 @@ gdn_prep_tc_kernel(const PrepArgs a) {
   {
     const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(a.k) + ((long)t0 * a.H + hq) * DK;
     const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(a.q) + ((long)t0 * a.H + hq) * DK;
+    // asynchronous copies, all in flight at once; rows past the chunk's
+    // tokens are zero-filled
     constexpr int PER = DK / 8;
     for (int idx = tid; idx < C * PER; idx += kThreads) {
       const int r = idx / PER, c8 = (idx % PER) * 8;
-      uint4 kv = make_uint4(0, 0, 0, 0), qv = make_uint4(0, 0, 0, 0);
-      if (r < L) {
-        kv = __ldg(reinterpret_cast<const uint4 *>(kg + (long)r * a.H * DK + c8));
-        qv = __ldg(reinterpret_cast<const uint4 *>(qg + (long)r * a.H * DK + c8));
-      }
-      *reinterpret_cast<uint4 *>(Kb + r * LDB + c8) = kv;
-      *reinterpret_cast<uint4 *>(Qb + r * LDB + c8) = qv;
+      const bool in = r < L;
+      const long off = (in ? (long)r * a.H * DK : 0) + c8;
+      sm100::cp_async16(sm100::smem_addr(Kb + r * LDB + c8), kg + off, in ? 16u : 0u);
+      sm100::cp_async16(sm100::smem_addr(Qb + r * LDB + c8), qg + off, in ? 16u : 0u);
     }
   }
-  bool positive = false;
   if constexpr (GATE == 0) {
     for (int r = tid; r < C; r += kThreads) {
-      const float gv = r < L ? __ldg(a.g + (long)(t0 + r) * a.HV + hv) : 0.f;
-      positive |= gv > 0.f;
-      Gs[r] = gv;
+      const bool in = r < L;
+      sm100::cp_async4(sm100::smem_addr(Gs + r), a.g + (long)(t0 + (in ? r : 0)) * a.HV + hv, in ? 4u : 0u);
     }
   } else {
     for (int idx = tid; idx < C * DK / 4; idx += kThreads) {
       const int r = idx / (DK / 4), c4 = (idx % (DK / 4)) * 4;
-      float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < L) gv = __ldg(reinterpret_cast<const float4 *>(a.g + ((long)(t0 + r) * a.HV + hv) * DK + c4));
-      positive |= (gv.x > 0.f) | (gv.y > 0.f) | (gv.z > 0.f) | (gv.w > 0.f);
-      *reinterpret_cast<float4 *>(Gs + r * LDG + c4) = gv;
+      const bool in = r < L;
+      sm100::cp_async16(sm100::smem_addr(Gs + r * LDG + c4), a.g + ((long)(t0 + (in ? r : 0)) * a.HV + hv) * DK + c4,
+                 in ? 16u : 0u);
     }
   }
-  for (int r = tid; r < C; r += kThreads)
-    Bs[r] = r < L ? __ldg(a.beta + (long)(t0 + r) * a.HV + hv) : 0.f;
+  for (int r = tid; r < C; r += kThreads) {
+    const bool in = r < L;
+    sm100::cp_async4(sm100::smem_addr(Bs + r), a.beta + (long)(t0 + (in ? r : 0)) * a.HV + hv, in ? 4u : 0u);
+  }
   for (int idx = tid; idx < C * LDC; idx += kThreads) Ts[idx] = 0.f;
+  sm100::cp_async_wait_all();
+  __syncthreads();
+  bool positive = false;
+  if constexpr (GATE == 0) {
+    for (int r = tid; r < C; r += kThreads) positive |= Gs[r] > 0.f;
+  } else {
+    for (int idx = tid; idx < C * DK; idx += kThreads) positive |= Gs[(idx / DK) * LDG + idx % DK] > 0.f;
+  }
   if (__syncthreads_or(positive) && tid == 0) atomicOr(a.flags, kFlagPositiveGate);
 
   // ---- cumulative log-gates ----
@@ -210,6 +220,75 @@ gdn_prep_tc_kernel(const PrepArgs a) {
         }
     }
   } else {
+    // Per 16-row block I with reference row o = 16 I:
+    //   A[r][s]   = beta_r sum_c (k_rc e^{b_rc - b_oc}) (k_sc e^{b_oc - b_sc})
+    //   Aqk[r][s] = scale  sum_c (q_rc e^{b_rc - b_oc}) (k_sc e^{b_oc - b_sc})
+    // r in the block, s <= o + 15: the row factors are <= 1, the column factors
+    // <= 1 for s <= o and at most e^{-(sum of the block's gates)} inside it.
+    // Products on the tensor cores in split tf32 (fp32-class accuracy).  When
+    // an in-block factor could leave the fp32 range the CTA falls back to
+    // forming every pairwise decay directly.
+    float *Xk = reinterpret_cast<float *>(smem + SM::kX);
+    float *Xq = Xk + 16 * SM::LDX;
+    float *Kh = Xq + 16 * SM::LDX;
+    constexpr int LDX = SM::LDX;
+    bool wide = false;
+    for (int idx = tid; idx < C * DK; idx += kThreads) {
+      const int s = idx / DK, c = idx % DK, o = s & ~15;
+      wide |= fabsf(Gs[o * LDG + c] - Gs[s * LDG + c]) > 80.f;
+    }
+    const bool pairwise = __syncthreads_or(wide);
+    if (!pairwise) {
+      for (int I = 0; I < C / 16; I++) {
+        const int o = 16 * I, ns = o + 16;  // columns s < ns
+        // four channels at a time
+        auto bf4 = [](const __nv_bfloat16 *p) {
+          const uint2 u = *reinterpret_cast<const uint2 *>(p);
+          const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+          const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+          return make_float4(lo.x, lo.y, hi.x, hi.y);
+        };
+        for (int idx = tid; idx < 16 * DK / 4; idx += kThreads) {
+          const int r = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
+          const float4 b = *reinterpret_cast<const float4 *>(Gs + (o + r) * LDG + c);
+          const float4 bo = *reinterpret_cast<const float4 *>(Gs + o * LDG + c);
+          const float4 e = make_float4(__expf(b.x - bo.x), __expf(b.y - bo.y), __expf(b.z - bo.z), __expf(b.w - bo.w));
+          const float4 kv = bf4(Kb + (o + r) * LDB + c), qv = bf4(Qb + (o + r) * LDB + c);
+          *reinterpret_cast<float4 *>(Xk + r * LDX + c) = make_float4(kv.x * e.x, kv.y * e.y, kv.z * e.z, kv.w * e.w);
+          *reinterpret_cast<float4 *>(Xq + r * LDX + c) = make_float4(qv.x * e.x, qv.y * e.y, qv.z * e.z, qv.w * e.w);
+        }
+        for (int idx = tid; idx < ns * DK / 4; idx += kThreads) {
+          const int r = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
+          const float4 b = *reinterpret_cast<const float4 *>(Gs + r * LDG + c);
+          const float4 bo = *reinterpret_cast<const float4 *>(Gs + o * LDG + c);
+          const float4 kv = bf4(Kb + r * LDB + c);
+          *reinterpret_cast<float4 *>(Kh + r * LDX + c) =
+              make_float4(kv.x * __expf(bo.x - b.x), kv.y * __expf(bo.y - b.y), kv.z * __expf(bo.z - b.z),
+                          kv.w * __expf(bo.w - b.w));
+        }
+        __syncthreads();
+        // tiles of 8 columns: ns / 8 for A, as many for Aqk
+        const int ntile = ns / 8;
+        for (int tile = warp; tile < 2 * ntile; tile += kThreads / 32) {
+          const bool isq = tile >= ntile;
+          const int n0 = 8 * (isq ? tile - ntile : tile);
+          const float *X = isq ? Xq : Xk;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f}, corr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+          for (int k0 = 0; k0 < DK; k0 += 8)
+            warp_mma_tf32x3(acc, corr, k0, [&](int m, int k) { return X[m * LDX + k]; },
+                            [&](int k, int n) { return Kh[(n0 + n) * LDX + k]; });
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const int r = o + acc_row(e), sc = n0 + acc_col(0, e);
+            const float v = acc[e] + corr[e];
+            if (isq) Aqks[r * LDC + sc] = sc <= r ? a.scale * v : 0.f;
+            else As[r * LDC + sc] = sc < r ? Bs[r] * v : 0.f;
+          }
+        }
+        __syncthreads();
+      }
+    } else {
     constexpr int NPAIR = C * (C + 1) / 2;
     for (int p = warp; p < NPAIR; p += kThreads / 32) {
       int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
@@ -232,6 +311,7 @@ gdn_prep_tc_kernel(const PrepArgs a) {
         As[r * LDC + s] = s < r ? Bs[r] * kk : 0.f;
         Aqks[r * LDC + s] = a.scale * qk;
       }
+    }
     }
     for (int idx = tid; idx < C * C; idx += kThreads) {
       const int r = idx / C, s = idx % C;

@@ -197,6 +197,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst_saddr, const void *src, 
                "r"(src_bytes)
                : "memory");
 }
+// wait for all of this thread's cp.async copies
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 // arrive on `bar` once this thread's earlier cp.async copies have landed
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
