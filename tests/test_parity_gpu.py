@@ -52,6 +52,19 @@ def test_shapes(dtype, gate_mode, chunk, dk, dv):
     check(c, synth.make_inputs(c))
 
 
+@pytest.mark.parametrize("gate_mode", [0, 1], ids=["gdn", "kda"])
+@pytest.mark.parametrize("chunk", [32, 64])
+def test_strong_decay(gate_mode, chunk):
+    """Log-gates down to -12 per token.  Within 16 tokens the decay can reach
+    e^-180: a factored in-block exponent would leave the fp32 range, so the
+    per-key prep must take its exact per-pair path, and cross-chunk state
+    contributions vanish."""
+    c = synth.Case(f"strong_decay_{gate_mode}_{chunk}", B=1, T=200, H=2, HV=4, dk=128,
+                   dv=128, chunk=chunk, dtype=torch.bfloat16, gate_mode=gate_mode,
+                   gate_dist="uniform", gate_low=-12.0, h0_std=0.1, seed=11)
+    check(c, synth.make_inputs(c))
+
+
 def test_tiny_fp32_workload():
     c = synth.case("gdn_fp32_t256")
     check(c, synth.make_inputs(c))
