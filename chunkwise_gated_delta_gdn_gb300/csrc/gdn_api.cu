@@ -75,6 +75,7 @@ struct Plan {
   long n_slots;   // chunk slots of the workspace
   size_t tile_bytes;
   size_t kq_bytes;
+  size_t decay_bytes;
   size_t ws_bytes;
 };
 
@@ -107,11 +108,17 @@ gdn_status plan(int B, int T, int H, int HV, int dk, int dv, int chunk,
   if (dtype == GDN_BF16)
     per = gate_mode == GDN_GATE_SCALAR ? (size_t)gdn::kLaImageBytes : (size_t)gdn::kPrepImageBytes;
   p.tile_bytes = (size_t)p.n_slots * (size_t)HV * per;
-  // bf16 scalar gate: the prep kernel also publishes the [K_next; Q] images
-  p.kq_bytes = (dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR)
-                   ? (size_t)p.n_slots * (size_t)H * (size_t)gdn::kq_image_bytes(dk)
-                   : 0;
-  p.ws_bytes = gdn::kWorkspaceHeader + p.tile_bytes + p.kq_bytes;
+  // bf16: the prep kernel also publishes key/query images, [K_next; Q] per
+  // (slot, q/k head) for the scalar gate, gated [K~; Q~] per (slot, value
+  // head) for the per-key gate, which also gets each chunk's per-channel decay
+  p.kq_bytes = 0;
+  p.decay_bytes = 0;
+  if (dtype == GDN_BF16) {
+    const size_t heads = gate_mode == GDN_GATE_SCALAR ? (size_t)H : (size_t)HV;
+    p.kq_bytes = (size_t)p.n_slots * heads * (size_t)gdn::kq_image_bytes(dk);
+    if (gate_mode == GDN_GATE_PER_KEY) p.decay_bytes = (size_t)p.n_slots * HV * dk * sizeof(float);
+  }
+  p.ws_bytes = gdn::kWorkspaceHeader + p.tile_bytes + p.kq_bytes + p.decay_bytes;
   return GDN_OK;
 }
 
@@ -198,6 +205,10 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
   unsigned char *kq_images =
       p.kq_bytes ? static_cast<unsigned char *>(workspace) + gdn::kWorkspaceHeader + p.tile_bytes
                  : nullptr;
+  float *decays = p.decay_bytes ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                            gdn::kWorkspaceHeader + p.tile_bytes +
+                                                            p.kq_bytes)
+                                : nullptr;
 
   gdn::ScanMaps maps;
   if (dtype == GDN_BF16 &&
@@ -211,6 +222,7 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
       pa.seq = seq; pa.H = H; pa.HV = HV; pa.scale = scale;
       pa.tiles = tiles; pa.flags = flags; pa.n_slots = (int)p.n_slots;
       pa.kq_images = kq_images;
+      pa.decays = decays;
       cudaError_t e;
       if (dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR)
         e = gdn::launch_prep_tmem(pa, maps, chunk, dk, stream);
@@ -226,6 +238,7 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
     sa.q = q; sa.k = k; sa.v = v; sa.g = g; sa.beta = beta; sa.h0 = h0;
     sa.o = o; sa.hT = hT; sa.seq = seq; sa.H = H; sa.HV = HV; sa.dv = dv;
     sa.scale = scale; sa.tiles = tiles; sa.flags = flags; sa.kq_images = kq_images;
+    sa.decays = decays;
     cudaError_t e;
     if (dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR)
       e = gdn::launch_scan_la(sa, maps, chunk, dk, stream);

@@ -49,7 +49,9 @@ struct PrepArgs {
   float *tiles;      // [n_slots][HV][2][C][C]: T = (I+A)^-1, then Aqk
   uint32_t *flags;   // device status word
   int n_slots;
-  unsigned char *kq_images;  // bf16 scalar gate: [K_next; Q] image per (slot, hq)
+  unsigned char *kq_images;  // bf16 scalar gate: [K_next; Q] image per (slot, hq);
+                             // bf16 per-key gate: gated [K~; Q~] image per (slot, hv)
+  float *decays;             // bf16 per-key gate: e^{b_last} per (slot, hv, key channel)
 };
 
 struct ScanArgs {
@@ -63,6 +65,7 @@ struct ScanArgs {
   const float *tiles;
   uint32_t *flags;
   const unsigned char *kq_images;  // as PrepArgs::kq_images (read by the scan)
+  const float *decays;             // as PrepArgs::decays
 };
 
 // Status-word bits (same values as GDN_FLAG_* in include/gdn.h).

@@ -357,6 +357,34 @@ gdn_prep_tc_kernel(const PrepArgs a) {
     __syncthreads();
   }
 
+  // ---- KDA: the scan's operands, published while b, K and Q are at hand:
+  //      the gated fp16 image [K~ = k e^b; Q~ = scale q e^b] (128 rows, K-major,
+  //      128-byte swizzle; rows past the tokens zero) and e^{b_last} ----
+  if constexpr (GATE == 1) {
+    unsigned char *kqi = a.kq_images + ((size_t)slot * a.HV + hv) * kq_image_bytes(DK);
+    constexpr int NCH = (DK / 64) * 128 * 8;  // 16-byte chunks of the image
+    for (int idx = tid; idx < NCH; idx += kThreads) {
+      const int p = idx >> 10, rr = (idx >> 3) & 127, phys = idx & 7;
+      const int half = rr >> 6, r = rr & 63;
+      const int c0 = p * 64 + ((phys ^ (rr & 7)) << 3);  // first channel of the chunk
+      uint4 out = make_uint4(0, 0, 0, 0);
+      if (r < L) {
+        const __nv_bfloat16 *src = (half ? Qb : Kb) + r * LDB + c0;
+        const float mul = half ? a.scale : 1.f;
+        __half2 *h = reinterpret_cast<__half2 *>(&out);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const float e0 = __expf(Gs[r * LDG + c0 + 2 * i]), e1 = __expf(Gs[r * LDG + c0 + 2 * i + 1]);
+          h[i] = __floats2half2_rn(mul * __bfloat162float(src[2 * i]) * e0,
+                                   mul * __bfloat162float(src[2 * i + 1]) * e1);
+        }
+      }
+      *reinterpret_cast<uint4 *>(kqi + p * 16384 + rr * 128 + phys * 16) = out;
+    }
+    for (int c = tid; c < DK; c += kThreads)
+      a.decays[((size_t)slot * a.HV + hv) * DK + c] = __expf(Gs[(C - 1) * LDG + c]);
+    __syncthreads();  // the gates below are overwritten in place
+  }
   // ---- KDA: Kt = k * exp(b_last - b) in place of the cumulative gates ----
   if constexpr (GATE == 1) {
     for (int c = tid; c < DK; c += kThreads) {

@@ -1,5 +1,7 @@
-// gdn_scan_tc.cu -- the serial-across-chunks scan kernel of the bf16 path, on
-// the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+// gdn_scan_tc.cu -- the serial-across-chunks scan kernel of the bf16
+// per-key-gate (KDA) path, on the 5th-generation tensor cores (tcgen05,
+// accumulators in tensor memory).  (The scalar-gate path runs the lookahead
+// scan of gdn_scan_la.cu; the GATE == 0 branches below are not instantiated.)
 //
 // One CTA per (sequence, value head, NS-column slice of dv), 384 threads:
 //  * warps 0-7 (the chain): warp w owns tensor-memory lanes / state rows
@@ -17,10 +19,9 @@
 //       O       = scale gam D1[queries] + D3     -> o, during D1 of chunk c+1
 //    Two tensor-core round trips per chunk sit on the serial path.
 //  * warps 8-11 (the producer) keep NST chunks in flight: one thread issues
-//    bulk copies of the chunk's fp16 [Kg; Qg] image (GDN: written by the prep
-//    kernel) and of the prep image (KDA: TMA tile loads of the bf16 keys and
-//    queries, converted and gated per channel in place); all fetch gates and
-//    beta with cp.async and form the per-row gate coefficients.
+//    bulk copies of the chunk's gated fp16 [Kg; Qg] image and of its [P1;
+//    AqkT] image, both written by the prep kernel; cp.async brings beta and
+//    the chunk's per-channel decay (also from the prep kernel).
 // V arrives by TMA into a two-deep ring of its own, two chunks ahead of its
 // use (issued by the chain as soon as a buffer has been consumed).  The split
 // over dv slices manufactures the parallelism a (batch, head) grid lacks
@@ -56,7 +57,7 @@ struct ScanTcSmem {
   static constexpr int PI = kPrepImageBytes;         // [P1; AqkT]
   static constexpr int SI = (DK / 8) * 1024;         // S, MN-major, dk K-rows
   static constexpr int YI = 8 * 1024;                // Y, MN-major, 64 K-rows (x2)
-  static constexpr int NRAW = GATE == 0 ? 2 * C : C * DK + C;  // gates, beta
+  static constexpr int NRAW = GATE == 0 ? 2 * C : DK + C;  // gates, beta / decays, beta
   static constexpr int NCOEF = GATE == 0 ? 3 * C + 4 : C + DK;
   static constexpr int kKQ = 0;
   static constexpr int kP = kKQ + NST * KQ;
@@ -75,7 +76,7 @@ struct ScanTcSmem {
   static constexpr int kBytes = kUsed + kSlack;
   // bytes landing per chunk: [Kg; Qg] (GDN: the prep's image; KDA: two TMA
   // boxes per panel) and the prep image
-  static constexpr uint32_t kTx = (GATE == 0 ? KQ : 2 * C * DK * 2) + PI;
+  static constexpr uint32_t kTx = KQ + PI;
   static_assert(KQ % 1024 == 0 && PI % 1024 == 0 && SI % 1024 == 0 && VI % 1024 == 0,
                 "1024-byte operand alignment");
   static_assert(kBytes <= 232448, "shared memory budget of one CTA");
@@ -273,8 +274,9 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       if (c > 0) {
         mbar_wait(bar_mma3, (c - 1) & 1, abort_flag);
         fence_after_sync();
-        if (query_warp) output_rows(c - 1);
+        // every product that read stage (c - 1) % NST has completed
         if (tid == 0) mbar_arrive(bar_empty + 8 * ((c - 1) % NST));
+        if (query_warp) output_rows(c - 1);
       }
       sgam_prev = sgam_r;
       mbar_wait(bar_mma1, c & 1, abort_flag);
@@ -364,12 +366,9 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       const uint32_t full = bar_full + 8 * s;
       if (pt == 0) {
         mbar_arrive_expect_tx(full, SM::kTx);
-        const uint32_t kq = smem_addr(sm + SM::kKQ + s * SM::KQ);
-#pragma unroll
-        for (int p = 0; p < DK / 64; p++) {
-          tma_load_3d(kq + p * 16384, &maps.k, p * 64, hq, t0, full);
-          tma_load_3d(kq + p * 16384 + 64 * 128, &maps.q, p * 64, hq, t0, full);
-        }
+        // the prep kernel's gated fp16 [K~; Q~] image of this chunk
+        bulk_g2s(smem_addr(sm + SM::kKQ + s * SM::KQ),
+                 a.kq_images + ((size_t)(base + c) * a.HV + hv) * SM::KQ, SM::KQ, full);
         const unsigned char *src = reinterpret_cast<const unsigned char *>(a.tiles) +
                                    ((size_t)(base + c) * a.HV + hv) * kPrepImageBytes;
         bulk_g2s(smem_addr(sm + SM::kP + s * SM::PI), src, kPrepImageBytes, full);
@@ -383,23 +382,19 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
           cp_async4(smem_addr(raw + C + pt), a.beta + row * a.HV + hv, in ? 4u : 0u);
         }
       } else {
-        for (int idx = pt; idx < C * DK / 4; idx += kProd) {
-          const int r = idx / (DK / 4), c4 = (idx % (DK / 4)) * 4;
-          const bool in = r < L;
-          const long row = in ? (long)(t0 + r) : (long)t0;
-          cp_async16(smem_addr(raw + r * DK + c4), a.g + (row * a.HV + hv) * DK + c4, in ? 16u : 0u);
-        }
+        // the chunk's per-channel decay (from the prep kernel) and beta
+        if (pt < DK / 4)
+          cp_async16(smem_addr(raw + 4 * pt), a.decays + ((size_t)(base + c) * a.HV + hv) * DK + 4 * pt, 16u);
         if (pt < C) {
           const bool in = pt < L;
           const long row = in ? (long)(t0 + pt) : (long)t0;
-          cp_async4(smem_addr(raw + C * DK + pt), a.beta + row * a.HV + hv, in ? 4u : 0u);
+          cp_async4(smem_addr(raw + DK + pt), a.beta + row * a.HV + hv, in ? 4u : 0u);
         }
       }
       cp_async_arrive_noinc(full);
     };
 
-    // chunk c landed: gate coefficients (and for KDA the gated fp16 keys and
-    // queries), then publish it
+    // chunk c landed: its coefficients, then publish it
     auto finish = [&](int c) {
       const int s = c % NST;
       const int t0 = start + c * C;
@@ -437,44 +432,8 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
           if (lane == 0) coef[3 * C] = __expf(blast);
         }
       } else {
-        // per key channel: cumulative gate -> exp in place; decay of the chunk
-        if (pt < DK) {
-          float run = 0.f;
-          bool positive = false;
-          for (int r = 0; r < C; r++) {
-            const float gk = raw[r * DK + pt];
-            positive |= gk > 0.f;
-            run += gk;
-            raw[r * DK + pt] = __expf(run);
-          }
-          coef[C + pt] = __expf(run);
-          if (positive) atomicOr(a.flags, kFlagPositiveGate);
-        }
-        if (pt < C) coef[pt] = raw[C * DK + pt];
-        named_bar(2, kProd);
-        // gated keys / queries: bf16 -> fp16 (k exp(b), scale q exp(b)) in place
-        constexpr int CH = (DK / 64) * 2 * C * 8;
-        for (int idx = pt; idx < CH; idx += kProd) {
-          const int p = idx / (2 * C * 8), rem = idx % (2 * C * 8);
-          const int half = rem / (C * 8), r = (rem / 8) % C, chunk = rem % 8;
-          const int row = half * 64 + r;
-          uint4 *ptr = reinterpret_cast<uint4 *>(kq + p * 16384 + row * 128 + chunk * 16);
-          const int col = p * 64 + ((chunk ^ (row & 7)) << 3);  // first channel of the chunk
-          uint4 v = *ptr, out = make_uint4(0, 0, 0, 0);
-          if (r < L) {
-            const float mul = half ? a.scale : 1.f;
-            const float *gm = raw + r * DK + col;
-            const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&v);
-            __half2 *h = reinterpret_cast<__half2 *>(&out);
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-              const float2 f = __bfloat1622float2(b[i]);
-              h[i] = __floats2half2_rn(mul * f.x * gm[2 * i], mul * f.y * gm[2 * i + 1]);
-            }
-          }
-          *ptr = out;
-        }
-        fence_proxy_async();
+        if (pt < DK) coef[C + pt] = raw[pt];
+        if (pt < C) coef[pt] = raw[DK + pt];
       }
       mbar_arrive(bar_ready + 8 * s);
     };

@@ -50,10 +50,10 @@ def test_workspace_query(lib):
     # image [P1; E; AqkT] + H x one 32 KB fp16 [K_next; Q] image)
     ws = gdn.gdn_chunk_fwd_workspace_bytes(1, 32768, 16, 48, 128, 128, 64, 0, 1, gdn.GDN_BF16)
     assert ws == 256 + (32768 // 64 + 1) * (48 * 256 * 128 + 16 * 2 * 128 * 128)
-    # bf16, per-key gate: one 24 KB image [P1; AqkT] per (slot, value head), no
-    # key/query images
+    # bf16, per-key gate: per (slot, value head) one 24 KB image [P1; AqkT], one
+    # 32 KB gated [K~; Q~] image and dk fp32 chunk decays
     ws = gdn.gdn_chunk_fwd_workspace_bytes(2, 8192, 32, 32, 128, 128, 32, 1, 2, gdn.GDN_BF16)
-    assert ws == 256 + (2 * 8192 // 32 + 2) * 32 * 192 * 128
+    assert ws == 256 + (2 * 8192 // 32 + 2) * 32 * (192 * 128 + 2 * 128 * 128 + 128 * 4)
     # fp32: header + slots x HV x (T and Aqk, C x C fp32)
     ws = gdn.gdn_chunk_fwd_workspace_bytes(1, 32768, 16, 48, 128, 128, 64, 0, 1, gdn.GDN_F32)
     assert ws == 256 + (32768 // 64 + 1) * 48 * 2 * 64 * 64 * 4
