@@ -1,8 +1,9 @@
-// gdn_prep_tc.cu -- the state-independent chunk-prep kernel of the bf16 path.
+// gdn_prep_tc.cu -- the state-independent chunk-prep kernel of the bf16
+// per-key-gate (KDA) path.  (The scalar gate runs gdn_prep_tmem.cu.)
 //
 // One CTA (128 threads) per (chunk slot, value head).  From the chunk's keys,
 // queries, gates and beta it forms, in fp32:
-//   b      cumulative natural-log gates (per key channel for KDA)
+//   b      cumulative natural-log gates, per key channel
 //   A      = strict-lower(beta_r sum_c k_rc k_sc exp(b_rc - b_sc))
 //   Aqk    = lower-incl-diag(scale sum_c q_rc k_sc exp(b_rc - b_sc))
 //   T      = (I + A)^-1   (blocked: 16 x 16 diagonal blocks by forward
@@ -17,8 +18,10 @@
 //   S <- diag(exp(b_last)) S + P1 Y     and     O = Qg S + AqkT Y,
 // the WY products W = T diag(beta) Kg and U = T diag(beta) V of stratat pull
 // #1296 ("What this is") folded into P1 and AqkT so that no dk-wide W ever
-// crosses HBM.  Every product here runs on the tensor cores in split bf16
-// (16-bit mantissa operands, fp32 accumulation); the images are the only
+// crosses HBM.  It also publishes the scan's gated operand image [Kg; Qg]
+// (Kg = k e^b, Qg = scale q e^b, fp16) and the chunk's per-channel decay
+// e^{b_last}.  Every product here runs on the tensor cores in split precision
+// (split tf32 or split bf16, fp32 accumulation); the images are the only
 // rounding to fp16.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -33,11 +36,11 @@ namespace {
 
 constexpr int kThreads = 128;
 
-template <int C, int DK, int GATE>
+template <int C, int DK>
 struct PrepTcSmem {
   static constexpr int LDB = DK + 8;  // bf16 row stride of K / Q
   static constexpr int LDC = C + 4;   // fp32 row stride of C x C tiles
-  static constexpr int LDG = GATE == 0 ? 1 : DK + 4;
+  static constexpr int LDG = DK + 4;
   // byte offsets
   static constexpr int kK = 0;
   static constexpr int kQ = kK + C * LDB * 2;  // Q, then (with A) the image
@@ -49,47 +52,25 @@ struct PrepTcSmem {
   static constexpr int kAqk = kA + C * LDC * 4;
   static constexpr int kT = kAqk + C * LDC * 4;
   static constexpr int kR = kT + C * LDC * 4;                  // 16 x LDC scratch
-  static constexpr int kG = kR + 16 * LDC * 4;                 // gates -> b -> Kt (KDA)
+  static constexpr int kG = kR + 16 * LDC * 4;                 // gates -> b -> Kt
   static constexpr int kBeta = kG + C * LDG * 4;
   static constexpr int kMeta = kBeta + C * 4;
-  // per-key gate: factored operands of one 16-row block (K~, Q~, then K^ for
+  // factored operands of one 16-row block (K~, Q~, then K^ for
   // up to C rows), fp32, row stride LDX
   static constexpr int LDX = DK + 4;
   static constexpr int kX = (kMeta + 16 + 15) / 16 * 16;
-  static constexpr int kBytes = GATE == 0 ? kMeta + 16 : kX + (32 + C) * LDX * 4;
+  static constexpr int kBytes = kX + (32 + C) * LDX * 4;
   static_assert(kImgSpan >= kPrepImageBytes, "image must fit the Q + A regions");
 };
-
-// acc[nt] += A * B over KDIM for a 16 x 8*NT tile; A row-major bf16 (exact),
-// B given as B^T row-major bf16 (i.e. B[k][n] = Bt[n][k]), both in shared memory
-template <int KDIM, int NT>
-__device__ __forceinline__ void mma_bf16_exact(float (&acc)[NT][4], const __nv_bfloat16 *A,
-                                               int lda, const __nv_bfloat16 *Bt, int ldb) {
-  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
-#pragma unroll 4
-  for (int k0 = 0; k0 < KDIM; k0 += 16) {
-    uint32_t a[4];
-    a[0] = *reinterpret_cast<const uint32_t *>(A + gq * lda + k0 + 2 * tq);
-    a[1] = *reinterpret_cast<const uint32_t *>(A + (gq + 8) * lda + k0 + 2 * tq);
-    a[2] = *reinterpret_cast<const uint32_t *>(A + gq * lda + k0 + 2 * tq + 8);
-    a[3] = *reinterpret_cast<const uint32_t *>(A + (gq + 8) * lda + k0 + 2 * tq + 8);
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++) {
-      const __nv_bfloat16 *b = Bt + (nt * 8 + gq) * ldb + k0 + 2 * tq;
-      mma16816(acc[nt], a, *reinterpret_cast<const uint32_t *>(b),
-               *reinterpret_cast<const uint32_t *>(b + 8));
-    }
-  }
-}
 
 __device__ __forceinline__ void put_f16(unsigned char *img, int row, int col, float v) {
   *reinterpret_cast<__half *>(img + sm100::kmajor_off(row, col, kPrepImageRows)) = __float2half_rn(v);
 }
 
-template <int C, int DK, int GATE>
+template <int C, int DK>
 __global__ void __launch_bounds__(kThreads)
 gdn_prep_tc_kernel(const PrepArgs a) {
-  using SM = PrepTcSmem<C, DK, GATE>;
+  using SM = PrepTcSmem<C, DK>;
   extern __shared__ __align__(16) unsigned char smem[];
   __nv_bfloat16 *Kb = reinterpret_cast<__nv_bfloat16 *>(smem + SM::kK);
   __nv_bfloat16 *Qb = reinterpret_cast<__nv_bfloat16 *>(smem + SM::kQ);
@@ -142,12 +123,7 @@ gdn_prep_tc_kernel(const PrepArgs a) {
       sm100::cp_async16(sm100::smem_addr(Qb + r * LDB + c8), qg + off, in ? 16u : 0u);
     }
   }
-  if constexpr (GATE == 0) {
-    for (int r = tid; r < C; r += kThreads) {
-      const bool in = r < L;
-      sm100::cp_async4(sm100::smem_addr(Gs + r), a.g + (long)(t0 + (in ? r : 0)) * a.HV + hv, in ? 4u : 0u);
-    }
-  } else {
+  {
     for (int idx = tid; idx < C * DK / 4; idx += kThreads) {
       const int r = idx / (DK / 4), c4 = (idx % (DK / 4)) * 4;
       const bool in = r < L;
@@ -163,29 +139,13 @@ gdn_prep_tc_kernel(const PrepArgs a) {
   sm100::cp_async_wait_all();
   __syncthreads();
   bool positive = false;
-  if constexpr (GATE == 0) {
-    for (int r = tid; r < C; r += kThreads) positive |= Gs[r] > 0.f;
-  } else {
+  {
     for (int idx = tid; idx < C * DK; idx += kThreads) positive |= Gs[(idx / DK) * LDG + idx % DK] > 0.f;
   }
   if (__syncthreads_or(positive) && tid == 0) atomicOr(a.flags, kFlagPositiveGate);
 
   // ---- cumulative log-gates ----
-  if constexpr (GATE == 0) {
-    if (warp == 0) {
-      float x0 = lane < C ? Gs[lane] : 0.f;
-      float x1 = lane + 32 < C ? Gs[lane + 32] : 0.f;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const float y0 = __shfl_up_sync(0xffffffffu, x0, d);
-        const float y1 = __shfl_up_sync(0xffffffffu, x1, d);
-        if (lane >= d) { x0 += y0; x1 += y1; }
-      }
-      x1 += __shfl_sync(0xffffffffu, x0, 31);
-      if (lane < C) Gs[lane] = x0;
-      if (lane + 32 < C) Gs[lane + 32] = x1;
-    }
-  } else {
+  {
     for (int c = tid; c < DK; c += kThreads) {
       float run = 0.f;
       for (int r = 0; r < C; r++) {
@@ -197,29 +157,7 @@ gdn_prep_tc_kernel(const PrepArgs a) {
   __syncthreads();
 
   // ---- A and Aqk ----
-  if constexpr (GATE == 0) {
-    // tasks: {K K^T, Q K^T} x row tiles of 16; all C columns (NT = C/8)
-    constexpr int NMT = C / 16, NT = C / 8;
-    for (int task = warp; task < 2 * NMT; task += kThreads / 32) {
-      const int which = task / NMT, m0 = (task % NMT) * 16;
-      float acc[NT][4] = {};
-      mma_bf16_exact<DK, NT>(acc, (which == 0 ? Kb : Qb) + m0 * LDB, LDB, Kb, LDB);
-#pragma unroll
-      for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const int r = m0 + acc_row(e), s = acc_col(nt, e);
-          float v = 0.f;
-          if (which == 0) {
-            if (s < r) v = Bs[r] * acc[nt][e] * __expf(Gs[r] - Gs[s]);
-            As[r * LDC + s] = v;
-          } else {
-            if (s <= r) v = a.scale * acc[nt][e] * __expf(Gs[r] - Gs[s]);
-            Aqks[r * LDC + s] = v;
-          }
-        }
-    }
-  } else {
+  {
     // Per 16-row block I with reference row o = 16 I:
     //   A[r][s]   = beta_r sum_c (k_rc e^{b_rc - b_oc}) (k_sc e^{b_oc - b_sc})
     //   Aqk[r][s] = scale  sum_c (q_rc e^{b_rc - b_oc}) (k_sc e^{b_oc - b_sc})
@@ -360,7 +298,7 @@ gdn_prep_tc_kernel(const PrepArgs a) {
   // ---- KDA: the scan's operands, published while b, K and Q are at hand:
   //      the gated fp16 image [K~ = k e^b; Q~ = scale q e^b] (128 rows, K-major,
   //      128-byte swizzle; rows past the tokens zero) and e^{b_last} ----
-  if constexpr (GATE == 1) {
+  {
     unsigned char *kqi = a.kq_images + ((size_t)slot * a.HV + hv) * kq_image_bytes(DK);
     constexpr int NCH = (DK / 64) * 128 * 8;  // 16-byte chunks of the image
     for (int idx = tid; idx < NCH; idx += kThreads) {
@@ -386,7 +324,7 @@ gdn_prep_tc_kernel(const PrepArgs a) {
     __syncthreads();  // the gates below are overwritten in place
   }
   // ---- KDA: Kt = k * exp(b_last - b) in place of the cumulative gates ----
-  if constexpr (GATE == 1) {
+  {
     for (int c = tid; c < DK; c += kThreads) {
       const float bl = Gs[(C - 1) * LDG + c];
       for (int r = 0; r < C; r++)
@@ -414,18 +352,13 @@ gdn_prep_tc_kernel(const PrepArgs a) {
           put_f16(img, kPrepImageRows - 64 + m0 + acc_row(e), n0 + acc_col(nt, e), acc[nt][e]);
     }
   }
-  // P1 = Kt^T T  (GDN: K exact, row-scaled T split; KDA: Kt split)
+  // P1 = Kt^T T  (Kt split)
   {
-    const float blast = GATE == 0 ? Gs[C - 1] : 0.f;
     constexpr int NMT = DK / 16, NNG = C / 32;
     for (int task = warp; task < NMT * NNG; task += kThreads / 32) {
       const int m0 = (task / NNG) * 16, n0 = (task % NNG) * 32;
       float acc[4][4] = {};
-      if constexpr (GATE == 0) {
-        warp_mma<C, 4, true, false>(
-            acc, [&](int m, int k) { return __bfloat162float(Kb[k * LDB + m0 + m]); },
-            [&](int k, int n) { return __expf(blast - Gs[k]) * Ts[k * LDC + n0 + n]; });
-      } else {
+      {
         warp_mma<C, 4, false, false>(
             acc, [&](int m, int k) { return Gs[k * LDG + m0 + m]; },
             [&](int k, int n) { return Ts[k * LDC + n0 + n]; });
@@ -445,10 +378,10 @@ gdn_prep_tc_kernel(const PrepArgs a) {
     dst[idx] = reinterpret_cast<const uint4 *>(img)[idx];
 }
 
-template <int C, int DK, int GATE>
+template <int C, int DK>
 cudaError_t launch_one(const PrepArgs &a, cudaStream_t stream) {
-  using SM = PrepTcSmem<C, DK, GATE>;
-  auto kern = gdn_prep_tc_kernel<C, DK, GATE>;
+  using SM = PrepTcSmem<C, DK>;
+  auto kern = gdn_prep_tc_kernel<C, DK>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
   if (err != cudaSuccess) return err;
@@ -459,10 +392,11 @@ cudaError_t launch_one(const PrepArgs &a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_prep_tc(const PrepArgs &a, int chunk, int dk, int gate, cudaStream_t stream) {
-  if (chunk == 64 && dk == 128) return gate ? launch_one<64, 128, 1>(a, stream) : launch_one<64, 128, 0>(a, stream);
-  if (chunk == 64 && dk == 64) return gate ? launch_one<64, 64, 1>(a, stream) : launch_one<64, 64, 0>(a, stream);
-  if (chunk == 32 && dk == 128) return gate ? launch_one<32, 128, 1>(a, stream) : launch_one<32, 128, 0>(a, stream);
-  if (chunk == 32 && dk == 64) return gate ? launch_one<32, 64, 1>(a, stream) : launch_one<32, 64, 0>(a, stream);
+  if (!gate) return cudaErrorInvalidValue;  // the scalar gate runs gdn_prep_tmem.cu
+  if (chunk == 64 && dk == 128) return launch_one<64, 128>(a, stream);
+  if (chunk == 64 && dk == 64) return launch_one<64, 64>(a, stream);
+  if (chunk == 32 && dk == 128) return launch_one<32, 128>(a, stream);
+  if (chunk == 32 && dk == 64) return launch_one<32, 64>(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -1,7 +1,7 @@
 // gdn_scan_tc.cu -- the serial-across-chunks scan kernel of the bf16
 // per-key-gate (KDA) path, on the 5th-generation tensor cores (tcgen05,
-// accumulators in tensor memory).  (The scalar-gate path runs the lookahead
-// scan of gdn_scan_la.cu; the GATE == 0 branches below are not instantiated.)
+// accumulators in tensor memory).  The scalar-gate path runs the lookahead
+// scan of gdn_scan_la.cu.
 //
 // One CTA per (sequence, value head, NS-column slice of dv), 384 threads:
 //  * warps 0-7 (the chain): warp w owns tensor-memory lanes / state rows
@@ -12,11 +12,13 @@
 //    Per chunk c (C rows, P1 and AqkT from the prep kernel's image):
 //       D1[c&1] = [Kg; Qg] S          one M=128 MMA (rows 0..63 keys,
 //                                     64..127 queries), K = dk
-//       Y       = diag(beta)(V - gam D1[keys])   -> fp16 B operand Y[c&1]
+//       Y       = diag(beta)(V - D1[keys])       -> fp16 B operand Y[c&1]
 //       D2      = P1 Y                S <- diag(exp(b_last)) S + D2
 //       D3      = AqkT Y              issued right behind D2; it runs during
 //                                     the state update, off the serial path
-//       O       = scale gam D1[queries] + D3     -> o, during D1 of chunk c+1
+//       O       = D1[queries] + D3               -> o, during D1 of chunk c+1
+//    (Kg = k e^b and Qg = scale q e^b per key channel, gated by the prep
+//    kernel; the state decays per key channel, S <- diag(e^{b_last}) S.)
 //    Two tensor-core round trips per chunk sit on the serial path.
 //  * warps 8-11 (the producer) keep NST chunks in flight: one thread issues
 //    bulk copies of the chunk's gated fp16 [Kg; Qg] image and of its [P1;
@@ -51,14 +53,14 @@ constexpr int NS = kScanTcSlice;
 constexpr int NH = NS / 2;  // columns per chain thread
 static_assert(NS == 64, "one 128-byte swizzle atom per S / Y row");
 
-template <int C, int DK, int GATE, int NST>
+template <int C, int DK, int NST>
 struct ScanTcSmem {
   static constexpr int KQ = (DK / 64) * 128 * 128;  // [Kg; Qg], K-major, 128 rows
   static constexpr int PI = kPrepImageBytes;         // [P1; AqkT]
   static constexpr int SI = (DK / 8) * 1024;         // S, MN-major, dk K-rows
   static constexpr int YI = 8 * 1024;                // Y, MN-major, 64 K-rows (x2)
-  static constexpr int NRAW = GATE == 0 ? 2 * C : DK + C;  // gates, beta / decays, beta
-  static constexpr int NCOEF = GATE == 0 ? 3 * C + 4 : C + DK;
+  static constexpr int NRAW = DK + C;   // decays, beta as landed
+  static constexpr int NCOEF = C + DK;  // beta, decays
   static constexpr int kKQ = 0;
   static constexpr int kP = kKQ + NST * KQ;
   static constexpr int kS = kP + NST * PI;
@@ -82,10 +84,10 @@ struct ScanTcSmem {
   static_assert(kBytes <= 232448, "shared memory budget of one CTA");
 };
 
-template <int C, int DK, int GATE, int NST>
+template <int C, int DK, int NST>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
-  using SM = ScanTcSmem<C, DK, GATE, NST>;
+  using SM = ScanTcSmem<C, DK, NST>;
   extern __shared__ unsigned char smem_raw[];
   // 1 KB-aligned base, as an offset into the shared array (the compiler then
   // knows every access below is to shared memory)
@@ -106,7 +108,6 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SM::kMisc + 4);
 
   const int n = blockIdx.x, hv = blockIdx.y, col0 = blockIdx.z * NS;
-  const int hq = hv / (a.HV / a.H);
 
   int start, end;
   bool ok = seq_ok(a.seq, n, start, end);
@@ -135,10 +136,6 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   }
   constexpr uint32_t kTmemCols = 256;  // D1 x2, D2, D3: 4 x NS columns
   if (warp == 0) tmem_alloc(smem_addr(tslot), kTmemCols);
-  if (GATE != 0) {
-    for (int i = tid; i < (NST * SM::KQ) / 16; i += kThreads)
-      reinterpret_cast<uint4 *>(sm + SM::kKQ)[i] = make_uint4(0, 0, 0, 0);
-  }
   for (int i = tid; i < (2 * SM::YI) / 16; i += kThreads)
     reinterpret_cast<uint4 *>(sm + SM::kY)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async();
@@ -197,7 +194,6 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     constexpr uint32_t idesc = idesc_f16(128, NS, 0, 1);
     const uint32_t sS = smem_addr(sm + SM::kS), sY = smem_addr(sm + SM::kY);
     bool nonfinite = false;
-    float sgam_prev = 0.f;  // scale * gam of this thread's query row, previous chunk
 
     // the 32 columns of this thread's lane at tensor-memory column `col`
     auto lane_half = [&](uint32_t col, float (&v)[NH]) {
@@ -224,8 +220,8 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
 #pragma unroll
           for (int i = 0; i < 4; i++) {
             const int j = ch * 8 + 2 * i;
-            const float v0 = (GATE == 0 ? sgam_prev * qs[j] : qs[j]) + d[j];
-            const float v1 = (GATE == 0 ? sgam_prev * qs[j + 1] : qs[j + 1]) + d[j + 1];
+            const float v0 = qs[j] + d[j];
+            const float v1 = qs[j + 1] + d[j + 1];
             nonfinite |= !(isfinite(v0) && isfinite(v1));
             pb[i] = __floats2bfloat162_rn(v0, v1);
           }
@@ -261,15 +257,9 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         mma_commit(bar_mma1);
       }
       // coefficients of this chunk (read before the stage is handed back)
-      float beta_r = 0.f, gam_r = 0.f, sgam_r = 0.f, dec = 0.f;
-      if constexpr (GATE == 0) {
-        const int r = t & 63;
-        if (r < C) { beta_r = coef[r]; gam_r = coef[C + r]; sgam_r = coef[2 * C + r]; }
-        dec = coef[3 * C];
-      } else {
-        if (t < C) beta_r = coef[t];
-        if (t < DK) dec = coef[C + t];
-      }
+      float beta_r = 0.f, dec = 0.f;
+      if (t < C) beta_r = coef[t];
+      if (t < DK) dec = coef[C + t];
       // the previous chunk's output and its stage, while D1 runs
       if (c > 0) {
         mbar_wait(bar_mma3, (c - 1) & 1, abort_flag);
@@ -278,7 +268,6 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         if (tid == 0) mbar_arrive(bar_empty + 8 * ((c - 1) % NST));
         if (query_warp) output_rows(c - 1);
       }
-      sgam_prev = sgam_r;
       mbar_wait(bar_mma1, c & 1, abort_flag);
       fence_after_sync();
 
@@ -297,8 +286,8 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
 #pragma unroll
           for (int i = 0; i < 4; i++) {
             const float2 vf = __bfloat1622float2(vb[i]);
-            const float xa = GATE == 0 ? gam_r * x[ch * 8 + 2 * i] : x[ch * 8 + 2 * i];
-            const float xb = GATE == 0 ? gam_r * x[ch * 8 + 2 * i + 1] : x[ch * 8 + 2 * i + 1];
+            const float xa = x[ch * 8 + 2 * i];
+            const float xb = x[ch * 8 + 2 * i + 1];
             ph[i] = __floats2half2_rn(beta_r * (vf.x - xa), beta_r * (vf.y - xb));
           }
           *reinterpret_cast<uint4 *>(sm + SM::kY + (c & 1) * SM::YI + mnmajor_chunk_off(t, c0 / 8 + ch, 64)) = pk;
@@ -374,22 +363,13 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         bulk_g2s(smem_addr(sm + SM::kP + s * SM::PI), src, kPrepImageBytes, full);
       }
       float *raw = reinterpret_cast<float *>(sm + SM::kRaw + s * SM::NRAW * 4);
-      if constexpr (GATE == 0) {
-        if (pt < C) {
-          const bool in = pt < L;
-          const long row = in ? (long)(t0 + pt) : (long)t0;
-          cp_async4(smem_addr(raw + pt), a.g + row * a.HV + hv, in ? 4u : 0u);
-          cp_async4(smem_addr(raw + C + pt), a.beta + row * a.HV + hv, in ? 4u : 0u);
-        }
-      } else {
-        // the chunk's per-channel decay (from the prep kernel) and beta
-        if (pt < DK / 4)
-          cp_async16(smem_addr(raw + 4 * pt), a.decays + ((size_t)(base + c) * a.HV + hv) * DK + 4 * pt, 16u);
-        if (pt < C) {
-          const bool in = pt < L;
-          const long row = in ? (long)(t0 + pt) : (long)t0;
-          cp_async4(smem_addr(raw + DK + pt), a.beta + row * a.HV + hv, in ? 4u : 0u);
-        }
+      // the chunk's per-channel decay (from the prep kernel) and beta
+      if (pt < DK / 4)
+        cp_async16(smem_addr(raw + 4 * pt), a.decays + ((size_t)(base + c) * a.HV + hv) * DK + 4 * pt, 16u);
+      if (pt < C) {
+        const bool in = pt < L;
+        const long row = in ? (long)(t0 + pt) : (long)t0;
+        cp_async4(smem_addr(raw + DK + pt), a.beta + row * a.HV + hv, in ? 4u : 0u);
       }
       cp_async_arrive_noinc(full);
     };
@@ -397,44 +377,11 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     // chunk c landed: its coefficients, then publish it
     auto finish = [&](int c) {
       const int s = c % NST;
-      const int t0 = start + c * C;
-      const int L = min(C, end - t0);
       mbar_wait(bar_full + 8 * s, (c / NST) & 1, abort_flag);
-      unsigned char *kq = sm + SM::kKQ + s * SM::KQ;
       float *raw = reinterpret_cast<float *>(sm + SM::kRaw + s * SM::NRAW * 4);
       float *coef = reinterpret_cast<float *>(sm + SM::kCoef + s * SM::NCOEF * 4);
-      if constexpr (GATE == 0) {
-        if (pt < 32) {
-          const float g0 = lane < C ? raw[lane] : 0.f;
-          const float g1 = lane + 32 < C ? raw[lane + 32] : 0.f;
-          if (__any_sync(0xffffffffu, g0 > 0.f || g1 > 0.f) && lane == 0) atomicOr(a.flags, kFlagPositiveGate);
-          float x0 = g0, x1 = g1;
-#pragma unroll
-          for (int d = 1; d < 32; d <<= 1) {
-            const float y0 = __shfl_up_sync(0xffffffffu, x0, d);
-            const float y1 = __shfl_up_sync(0xffffffffu, x1, d);
-            if (lane >= d) { x0 += y0; x1 += y1; }
-          }
-          x1 += __shfl_sync(0xffffffffu, x0, 31);
-          const float blast = __shfl_sync(0xffffffffu, C > 32 ? x1 : x0, (C - 1) & 31);
-          if (lane < C) {
-            const float gm = __expf(x0);
-            coef[lane] = raw[C + lane];
-            coef[C + lane] = gm;
-            coef[2 * C + lane] = a.scale * gm;
-          }
-          if (lane + 32 < C) {
-            const float gm = __expf(x1);
-            coef[lane + 32] = raw[C + lane + 32];
-            coef[C + lane + 32] = gm;
-            coef[2 * C + lane + 32] = a.scale * gm;
-          }
-          if (lane == 0) coef[3 * C] = __expf(blast);
-        }
-      } else {
-        if (pt < DK) coef[C + pt] = raw[pt];
-        if (pt < C) coef[pt] = raw[DK + pt];
-      }
+      if (pt < DK) coef[C + pt] = raw[pt];
+      if (pt < C) coef[pt] = raw[DK + pt];
       mbar_arrive(bar_ready + 8 * s);
     };
 
@@ -453,10 +400,10 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int C, int DK, int GATE, int NST>
+template <int C, int DK, int NST>
 cudaError_t launch_one(const ScanArgs &a, const ScanMaps &maps, cudaStream_t stream) {
-  using SM = ScanTcSmem<C, DK, GATE, NST>;
-  auto kern = gdn_scan_tc_kernel<C, DK, GATE, NST>;
+  using SM = ScanTcSmem<C, DK, NST>;
+  auto kern = gdn_scan_tc_kernel<C, DK, NST>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
   if (err != cudaSuccess) return err;
@@ -466,10 +413,9 @@ cudaError_t launch_one(const ScanArgs &a, const ScanMaps &maps, cudaStream_t str
 
 template <int C, int DK>
 cudaError_t dispatch_gate(const ScanArgs &a, const ScanMaps &m, int gate, cudaStream_t s) {
-  // the scalar gate runs the lookahead scan (gdn_scan_la.cu); two stages in
-  // flight for the per-key gate, whose per-channel gates take a stage's room
+  // per-key gate only (the scalar gate runs gdn_scan_la.cu); two stages in flight
   if (!gate) return cudaErrorInvalidValue;
-  return launch_one<C, DK, 1, 2>(a, m, s);
+  return launch_one<C, DK, 2>(a, m, s);
 }
 
 }  // namespace
