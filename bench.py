@@ -224,6 +224,9 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world, c0, wl, config)
         return
+    if c0.T == 1 and "decode" in c0.name:
+        bench_decode(args, rank, world, local_rank, c0, wl, config)
+        return
 
     import torch
     import torch.distributed as dist
@@ -444,6 +447,145 @@ def main():
             "roofline": roofline, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": 2 * K,
             "kernels_ms": {"prep": prep_ms, "scan": scan_ms}, "device_flags": flags}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def decode_bytes(c):
+    """HBM bytes one decode step must move: every state read and written once,
+    plus q, k, v, g, beta read and o written."""
+    es = 2 if str(c.dtype).endswith("bfloat16") else 4
+    n = c.B
+    state = n * c.HV * c.dk * c.dv * 4
+    qk = 2 * n * c.H * c.dk * es
+    vo = 2 * n * c.HV * c.dv * es
+    gb = n * c.HV * ((1 if c.gate_mode == 0 else c.dk) + 1) * 4
+    return 2 * state + qk + vo + gb
+
+
+def bench_decode(args, rank, world, local_rank, c0, wl, config):
+    """One decode step (T = 1) of a batch of sequences through the token-serial
+    kernel, the states updated in place on the device as a serving loop keeps
+    them.  Tokens/s = sequences per step / step time."""
+    import torch
+    import torch.distributed as dist
+
+    from chunkwise_gated_delta_gdn_gb300 import build as cuda_build
+    from chunkwise_gated_delta_gdn_gb300 import gdn, synth
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    gdn.load(cuda_build.build())
+    x = synth.make_inputs(c0)
+    names = ("q", "k", "v", "g", "beta")
+    d = {n: x[n].to(dev) for n in names}
+    state = x["h0"].to(dev)
+    o = torch.empty((c0.B, 1, c0.HV, c0.dv), dtype=c0.dtype, device=dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(dd, ob):
+        gdn.gdn_recurrent_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], state, hT=state,
+                              o=ob, scale=c0.scale)
+
+    gdn.gdn_recurrent_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], state, hT=state, o=o,
+                          scale=c0.scale, flags=flags)
+    dev_flags = gdn.gdn_read_device_flags(flags)
+    for _ in range(args.warmup):
+        step(d, o)
+    torch.cuda.synchronize()
+    K = args.steps
+    main = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.25)
+    a.record(main)
+    for _ in range(K):
+        step(d, o)
+    b.record(main)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_step = a.elapsed_time(b) / K
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * c0.B / (ms_step / 1e3)
+
+    # end to end: each step's token inputs copied in from pinned host memory
+    # and its outputs o copied back; the states stay resident on the device
+    e2e = None
+    if not args.no_e2e:
+        host = {n: x[n].pin_memory() for n in names}
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = o.numel() * o.element_size()
+        for _ in range(3):
+            for n in names:
+                d[n].copy_(host[n], non_blocking=True)
+            step(d, o)
+            o_host.copy_(o, non_blocking=True)
+        torch.cuda.synchronize()
+        a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a2.record(main)
+        for _ in range(args.e2e_steps):
+            for n in names:
+                d[n].copy_(host[n], non_blocking=True)
+            step(d, o)
+            o_host.copy_(o, non_blocking=True)
+        b2.record(main)
+        torch.cuda.synchronize()
+        e2e_ms = a2.elapsed_time(b2) / args.e2e_steps
+        e2e = {"value": world * c0.B / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms, "steps": args.e2e_steps,
+               "note": "token inputs in and o out every step on one stream; the states "
+                       "stay resident on the device"}
+
+    peaks, peak_src = load_peaks()
+    kbytes = decode_bytes(c0)
+    achieved = kbytes / (ms_step / 1e3) / 1e9
+    traffic, traffic_note = measured_traffic(c0.name, "recurrent", c0.B)
+    roofline = {"bound": "hbm", "kernel": "gdn_recurrent_kernel", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": traffic, "algorithmic_bytes": kbytes, "kernel_ms": ms_step,
+                "peak_source": f"hbm_gbs of {peak_src}"}
+    if traffic_note:
+        roofline["traffic_note"] = traffic_note
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t0, n_done = time.perf_counter(), 0
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 10.0) or n_done == 0:
+            _, n = oracle_sample(wl, x, 1)
+            n_done += n
+        sec = time.perf_counter() - t0
+        cpu = {"value": n_done / sec, "unit": UNIT, "cores": oracle.num_threads(),
+               "kind": "oracle",
+               "sample": f"fp64 token-serial oracle, {n_done // c0.B} whole decode steps of "
+                         f"{c0.name} ({c0.B} sequences x {c0.HV} value heads), {sec:.1f} s"}
+
+    line = {"metric": "decode tokens/s (gated delta-rule step, T = 1, 1 GB300) and % of HBM "
+                      "roofline",
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype_name, "data": "synthetic (seeded; no dataset)",
+            "config": dict(config, l2="states exceed the 129 MB L2; no flush",
+                           parallelism=f"replicas x{world}",
+                           state="updated in place (hT = h0), resident on the device"),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": K, "device_flags": dev_flags}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -1,8 +1,8 @@
 // gdn_api.cu -- host side of the C ABI declared in include/gdn.h: argument
 // validation, workspace sizing and the two launches (prep, then scan) on the
-// caller's stream.  Unsupported requests are refused explicitly, before
-// anything is enqueued (logismos issue #46, "Acceptance": unsupported inputs
-// fail explicitly).
+// caller's stream, and the one launch of the token-serial form.  Unsupported
+// requests are refused explicitly, before anything is enqueued (logismos
+// issue #46, "Acceptance": unsupported inputs fail explicitly).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -283,6 +283,71 @@ gdn_status gdn_chunk_fwd_scan(const void *q, const void *k, const void *v, const
                               gdn_stream_t stream) {
   return run(kScan, q, k, v, g, beta, h0, o, hT, cu_seqlens, n_seqs, B, T, H, HV, dk, dv,
              chunk, scale, gate_mode, dtype, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_recurrent_fwd(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, const float *h0, void *o, float *hT,
+                             const int32_t *cu_seqlens, int n_seqs, int B, int T, int H,
+                             int HV, int dk, int dv, float scale, int gate_mode, int dtype,
+                             uint32_t *flags, gdn_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (B <= 0 || T < 0 || H <= 0 || HV <= 0 || dk <= 0 || dv <= 0) return GDN_ERR_INVALID_ARG;
+  if (HV % H != 0 || HV > 65535) return GDN_ERR_INVALID_ARG;
+  if (gate_mode != GDN_GATE_SCALAR && gate_mode != GDN_GATE_PER_KEY) return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GDN_ERR_INVALID_ARG;
+  const bool packed = cu_seqlens != nullptr;
+  int n_states;
+  if (packed) {
+    if (B != 1 || n_seqs <= 0) return GDN_ERR_INVALID_ARG;
+    n_states = n_seqs;
+  } else {
+    if (n_seqs != 0 && n_seqs != B) return GDN_ERR_INVALID_ARG;
+    n_states = B;
+  }
+  if (!(dk == 64 || dk == 128) || dv % 32 != 0 || dv > 1024) return GDN_ERR_UNSUPPORTED;
+  const long Ttot = (long)B * T;
+  if (Ttot > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+
+  if (Ttot > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, g, beta, h0, o, hT, cu_seqlens};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+  if (flags && (reinterpret_cast<uintptr_t>(flags) & 3u) != 0) return GDN_ERR_INVALID_ARG;
+
+  // aliasing: hT may be h0 itself (an in-place state update), not a part of it;
+  // o, hT and the status word overlap no input and no other output
+  const size_t es = dtype == GDN_BF16 ? 2 : 4;
+  const size_t n_qk = (size_t)Ttot * H * dk * es;
+  const size_t n_vo = (size_t)Ttot * HV * dv * es;
+  const size_t n_g = (size_t)Ttot * HV * (gate_mode == GDN_GATE_PER_KEY ? dk : 1) * 4;
+  const size_t n_b = (size_t)Ttot * HV * 4;
+  const size_t n_h = (size_t)n_states * HV * dk * dv * 4;
+  const size_t n_cu = packed ? ((size_t)n_seqs + 1) * 4 : 0;
+  if (hT != h0 && overlap(hT, n_h, h0, n_h)) return GDN_ERR_INVALID_ARG;
+  const void *ins[] = {q, k, v, g, beta, cu_seqlens};
+  const size_t in_n[] = {n_qk, n_qk, n_vo, n_g, n_b, n_cu};
+  for (int i = 0; i < 6; i++) {
+    if (overlap(o, n_vo, ins[i], in_n[i]) || overlap(hT, n_h, ins[i], in_n[i]) ||
+        overlap(flags, 4, ins[i], in_n[i]))
+      return GDN_ERR_INVALID_ARG;
+  }
+  if (overlap(o, n_vo, h0, n_h) || overlap(o, n_vo, hT, n_h) || overlap(flags, 4, o, n_vo) ||
+      overlap(flags, 4, h0, n_h) || overlap(flags, 4, hT, n_h))
+    return GDN_ERR_INVALID_ARG;
+
+  if (flags && cudaMemsetAsync(flags, 0, sizeof(uint32_t), stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  gdn::RecurrentArgs ra;
+  ra.q = q; ra.k = k; ra.v = v; ra.g = g; ra.beta = beta; ra.h0 = h0;
+  ra.o = o; ra.hT = hT;
+  ra.seq.cu = cu_seqlens;
+  ra.seq.n_seqs = n_states;
+  ra.seq.T = T;
+  ra.seq.Ttot = (int)Ttot;
+  ra.H = H; ra.HV = HV; ra.dv = dv; ra.scale = scale; ra.flags = flags;
+  if (gdn::launch_recurrent(ra, dk, dtype, gate_mode, stream) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
 }
 
 gdn_status gdn_read_device_flags(const void *workspace, uint32_t *flags_out,

@@ -1,5 +1,5 @@
 // gdn_internal.h -- declarations shared by the host API (gdn_api.cu) and the
-// kernel translation units (gdn_prep.cu, gdn_scan.cu).  Not part of the ABI.
+// kernel translation units.  Not part of the ABI.
 #pragma once
 
 #include <cuda.h>
@@ -68,6 +68,19 @@ struct ScanArgs {
   const float *decays;             // as PrepArgs::decays
 };
 
+// The token-serial form (gdn_recurrent.cu): state in registers, one token at
+// a time; hT may be h0 itself.
+struct RecurrentArgs {
+  const void *q, *k, *v;
+  const float *g, *beta, *h0;
+  void *o;
+  float *hT;
+  SeqInfo seq;
+  int H, HV, dv;
+  float scale;
+  uint32_t *flags;  // device status word, or nullptr
+};
+
 // Status-word bits (same values as GDN_FLAG_* in include/gdn.h).
 constexpr uint32_t kFlagPositiveGate = 1u << 0;
 constexpr uint32_t kFlagNonfinite = 1u << 1;
@@ -101,5 +114,8 @@ cudaError_t launch_prep_tmem(const PrepArgs &a, const ScanMaps &maps, int chunk,
                              cudaStream_t stream);
 cudaError_t launch_scan_la(const ScanArgs &a, const ScanMaps &maps, int chunk, int dk,
                            cudaStream_t stream);
+// token-serial form; dv a multiple of 32
+cudaError_t launch_recurrent(const RecurrentArgs &a, int dk, int dtype, int gate,
+                             cudaStream_t stream);
 
 }  // namespace gdn

@@ -37,7 +37,7 @@ GDN_FLAG_TIMEOUT = 1 << 3
 # every symbol include/gdn.h declares
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_chunk_fwd_workspace_bytes",
             "gdn_chunk_fwd", "gdn_chunk_fwd_prep", "gdn_chunk_fwd_scan",
-            "gdn_chunk_fwd_noalloc", "gdn_read_device_flags")
+            "gdn_chunk_fwd_noalloc", "gdn_recurrent_fwd", "gdn_read_device_flags")
 
 _lock = threading.Lock()
 _lib = None
@@ -81,6 +81,9 @@ def load(path: Optional[str] = None):
                                               i32, i32, i32, i32, i32, i32, f32, i32, i32,
                                               vp]
         lib.gdn_chunk_fwd_noalloc.restype = i32
+        lib.gdn_recurrent_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                          i32, i32, i32, i32, f32, i32, i32, vp, vp]
+        lib.gdn_recurrent_fwd.restype = i32
         lib.gdn_read_device_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gdn_read_device_flags.restype = i32
         _lib = lib
@@ -198,9 +201,69 @@ def gdn_chunk_fwd_scan(q, k, v, g, beta, h0=None, *, workspace: torch.Tensor,
           hT is not None, workspace, stream)
 
 
+def gdn_recurrent_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                      beta: torch.Tensor, h0: Optional[torch.Tensor] = None, *,
+                      scale: Optional[float] = None,
+                      cu_seqlens: Optional[torch.Tensor] = None,
+                      o: Optional[torch.Tensor] = None, hT: Optional[torch.Tensor] = None,
+                      output_final_state: bool = True,
+                      flags: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None
+                      ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Token-serial form (the decode step when T == 1); returns ``(o, hT)``.
+
+    Same tensors as :func:`gdn_chunk_fwd`; dv any multiple of 32 up to 1024.
+    Pass ``hT=h0`` to update the state in place.  ``flags``: an int32/uint32
+    device tensor of at least one element that receives the GDN_FLAG_* bits
+    (read it with :func:`gdn_read_device_flags`), or None.
+    """
+    lib = load()
+    B, T, H, dk = q.shape
+    HV, dv = v.shape[2], v.shape[3]
+    if k.shape != q.shape or v.shape[:2] != (B, T) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v: inconsistent shapes or dtypes")
+    if g.dim() == 3:
+        gate_mode = GDN_GATE_SCALAR
+    elif g.dim() == 4:
+        gate_mode = GDN_GATE_PER_KEY
+    else:
+        raise ValueError("g must be [B,T,HV] or [B,T,HV,dk]")
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("h0", h0),
+                    ("cu_seqlens", cu_seqlens), ("o", o), ("hT", hT), ("flags", flags)):
+        if t is not None and (t.device != dev or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous tensor on {dev}")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    if h0 is not None and h0.dtype != torch.float32:
+        raise TypeError("h0 must be float32")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if flags is not None and (flags.element_size() != 4 or flags.numel() < 1):
+        raise TypeError("flags must hold at least one 4-byte element")
+    n_seqs = int(cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    dt = _dtype_code(q.dtype)
+    if scale is None:
+        scale = dk ** -0.5
+    if o is None:
+        o = torch.empty((B, T, HV, dv), dtype=q.dtype, device=dev)
+    if hT is None and output_final_state:
+        hT = torch.empty((n_seqs, HV, dk, dv), dtype=torch.float32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    status = lib.gdn_recurrent_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(hT),
+        _ptr(cu_seqlens), n_seqs, B, T, H, HV, dk, dv, float(scale), gate_mode, dt,
+        _ptr(flags), ctypes.c_void_p(stream.cuda_stream))
+    if status != GDN_OK:
+        raise GdnError(status, "gdn_recurrent_fwd")
+    return o, hT
+
+
 def gdn_read_device_flags(workspace: torch.Tensor,
                           stream: Optional[torch.cuda.Stream] = None) -> int:
-    """Status word (GDN_FLAG_*) of the last call that used ``workspace``."""
+    """Status word (GDN_FLAG_*) of the last call that used ``workspace`` (or,
+    for gdn_recurrent_fwd, the ``flags`` tensor)."""
     lib = load()
     if stream is None:
         stream = torch.cuda.current_stream(workspace.device)

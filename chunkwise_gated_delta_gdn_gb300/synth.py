@@ -94,6 +94,17 @@ WORKLOADS = {
                                dtype=torch.bfloat16, gate_mode=GATE_SCALAR,
                                gate_dist="uniform", gate_low=-5.0, h0_std=0.1,
                                n_seqs=8),
+    # one decode step (T = 1) for a batch of 256 sequences at the 32k spot's
+    # head geometry: the one-token grouped step of logismos issue #46
+    # ("Verified implementation boundary"); the states (805 MB) dominate
+    "gdn_decode_bf16_b256": Case("gdn_decode_bf16_b256", B=256, T=1, H=16, HV=48,
+                                 dk=128, dv=128, chunk=64, dtype=torch.bfloat16,
+                                 gate_mode=GATE_SCALAR, gate_dist="uniform",
+                                 gate_low=-5.0, h0_std=0.1),
+    "kda_decode_bf16_b256": Case("kda_decode_bf16_b256", B=256, T=1, H=32, HV=32,
+                                 dk=128, dv=128, chunk=32, dtype=torch.bfloat16,
+                                 gate_mode=GATE_PER_KEY, gate_dist="uniform",
+                                 gate_low=-5.0, h0_std=0.1),
 }
 
 

@@ -198,6 +198,37 @@ GDN_API gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k, const voi
                                  gdn_stream_t stream);
 
 /*
+ * The token-serial (recurrent) form of the same recurrence: each sequence's
+ * tokens one after another, the state held on chip between them.  With T == 1
+ * this is the decode step (logismos issue #46, "Verified implementation
+ * boundary": a one-token grouped step, K-first input state, separate output
+ * and next-state buffers, value width up to 1024); with T > 1 it is the
+ * plain definition that gdn_chunk_fwd reaches by the chunked route, useful
+ * for short prompts and continuation of a few tokens.
+ *
+ * Arguments, layouts and the grouped-head mapping are those of gdn_chunk_fwd,
+ * without chunk and workspace.  Differences:
+ *  - dk in {64, 128}; dv any multiple of 32 up to 1024.
+ *  - hT may be h0 itself (the same pointer): the state is then updated in
+ *    place, as a decode loop over a state cache wants.  Any other overlap of
+ *    hT with h0 is refused.
+ *  - flags: a DEVICE pointer to one uint32 (4-byte aligned) or NULL.  When
+ *    given, the call clears it, then sets GDN_FLAG_* bits as gdn_chunk_fwd
+ *    does in its workspace (POSITIVE_GATE, NONFINITE, BAD_SEQLENS);
+ *    gdn_read_device_flags(flags, ...) reads it back.
+ * No workspace is needed and nothing else is written.
+ *
+ * Numerics: fp32 state and arithmetic throughout (no tensor-core operands),
+ * o rounded once to dtype.
+ */
+GDN_API gdn_status gdn_recurrent_fwd(const void *q, const void *k, const void *v,
+                                     const float *g, const float *beta, const float *h0,
+                                     void *o, float *hT, const int32_t *cu_seqlens,
+                                     int n_seqs, int B, int T, int H, int HV, int dk,
+                                     int dv, float scale, int gate_mode, int dtype,
+                                     uint32_t *flags, gdn_stream_t stream);
+
+/*
  * Copy the device status word of `workspace` to *flags_out (host pointer)
  * after all work queued on `stream` so far has finished (synchronises the
  * stream).  Returns GDN_ERR_INVALID_ARG for NULL arguments and GDN_ERR_CUDA

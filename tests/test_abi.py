@@ -126,3 +126,42 @@ def test_binding_refuses_to_run_without_library(tmp_path):
             gdn.load(str(tmp_path / "missing.so"))
         finally:
             gdn._lib = saved
+
+
+def call_rec(lib, **kw):
+    a = dict(q=addr(0), k=addr(1), v=addr(2), g=addr(3), beta=addr(4), h0=addr(5),
+             o=addr(6), hT=addr(7), cu=None, n_seqs=1, B=1, T=1, H=2, HV=4, dk=128,
+             dv=128, scale=0.088, gate_mode=0, dtype=1, flags=addr(8))
+    a.update(kw)
+    return lib.gdn_recurrent_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["o"],
+                                 a["hT"], a["cu"], a["n_seqs"], a["B"], a["T"], a["H"],
+                                 a["HV"], a["dk"], a["dv"], a["scale"], a["gate_mode"],
+                                 a["dtype"], a["flags"], None)
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(q=None), gdn.GDN_ERR_INVALID_ARG),
+    (dict(o=None), gdn.GDN_ERR_INVALID_ARG),
+    (dict(B=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(T=-1), gdn.GDN_ERR_INVALID_ARG),
+    (dict(H=3), gdn.GDN_ERR_INVALID_ARG),
+    (dict(gate_mode=2), gdn.GDN_ERR_INVALID_ARG),
+    (dict(dtype=7), gdn.GDN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), gdn.GDN_ERR_INVALID_ARG),
+    (dict(dk=96), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dk=256), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dv=48), gdn.GDN_ERR_UNSUPPORTED),          # not a multiple of 32
+    (dict(dv=2048), gdn.GDN_ERR_UNSUPPORTED),        # above 1024
+    (dict(q=ctypes.c_void_p(BASE + 8)), gdn.GDN_ERR_INVALID_ARG),
+    (dict(flags=ctypes.c_void_p(BASE + 8 * STRIDE + 2)), gdn.GDN_ERR_INVALID_ARG),
+    (dict(hT=ctypes.c_void_p(BASE + 5 * STRIDE + 4096)), gdn.GDN_ERR_INVALID_ARG),  # partial overlap
+    (dict(o=addr(2)), gdn.GDN_ERR_INVALID_ARG),     # o aliases v
+    (dict(o=addr(5)), gdn.GDN_ERR_INVALID_ARG),     # o aliases h0
+    (dict(flags=addr(7)), gdn.GDN_ERR_INVALID_ARG),  # status word inside hT
+    (dict(hT=addr(1)), gdn.GDN_ERR_INVALID_ARG),    # hT aliases k
+    (dict(cu=addr(9), B=2, n_seqs=2), gdn.GDN_ERR_INVALID_ARG),
+    (dict(cu=addr(9), n_seqs=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(B=2, n_seqs=3), gdn.GDN_ERR_INVALID_ARG),
+])
+def test_recurrent_refusals(lib, kw, status):
+    assert call_rec(lib, **kw) == status
