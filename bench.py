@@ -84,10 +84,13 @@ def load_peaks():
         return dict(PEAKS_FALLBACK), "fallback"
 
 
-def kernel_source_sha():
+def kernel_source_sha(source):
+    """Hash of one kernel's translation unit and every header of csrc/ (the
+    structs and device helpers it compiles with)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunkwise_gated_delta_gdn_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = [source] + sorted(n for n in os.listdir(csrc) if n.endswith((".h", ".cuh")))
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -104,7 +107,9 @@ def measured_traffic(workload, kernel, units):
     except Exception:
         return None, None
     for e in rec.get("entries", []):
-        if e.get("kernel") == kernel and e.get("source_sha") == kernel_source_sha():
+        src = e.get("source")
+        if (e.get("kernel") == kernel and e.get("workload") == workload and src
+                and e.get("source_sha") == kernel_source_sha(src)):
             per_unit = float(e["dram_bytes"]) / float(e["tokens"])
             return per_unit * units, e.get("note")
     return None, None
