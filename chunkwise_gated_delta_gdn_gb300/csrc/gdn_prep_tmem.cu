@@ -160,25 +160,41 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   };
   fetch(wg);
   mbar_wait(bar_tma, 0, abort_flag);
-  // bf16 -> fp16 in place; rows beyond each tile's tokens -> 0
+  // bf16 -> fp16 in place; rows beyond each tile's tokens -> 0.  Six 16-byte
+  // chunks per thread in flight at a time (the loop is shared-memory latency
+  // bound otherwise).
   {
     constexpr int CH = (DK / 64) * 3 * C * 8;
-    for (int idx = tid; idx < CH; idx += NT) {
-      const int p = idx / (3 * C * 8), rem = idx % (3 * C * 8);
-      const int third = rem / (C * 8), r = (rem / 8) % C, chunk = rem % 8;
-      uint4 *ptr = reinterpret_cast<uint4 *>(kq + p * SM::PANEL + (third * 64 + r) * 128 + chunk * 16);
-      uint4 out = make_uint4(0, 0, 0, 0);
-      if (r < (third == 2 ? Ln : L)) {
-        const uint4 v = *ptr;
-        const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&v);
-        __half2 *h = reinterpret_cast<__half2 *>(&out);
+    constexpr int PER = CH / NT, UNR = 6;
+    static_assert(CH % NT == 0 && PER % UNR == 0, "conversion tiling");
+#pragma unroll 1
+    for (int b0 = 0; b0 < PER; b0 += UNR) {
+      uint4 v[UNR];
+      uint4 *ptr[UNR];
+      bool keep[UNR];
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-          const float2 f = __bfloat1622float2(b[i]);
-          h[i] = __floats2half2_rn(f.x, f.y);
-        }
+      for (int u = 0; u < UNR; u++) {
+        const int idx = tid + (b0 + u) * NT;
+        const int p = idx / (3 * C * 8), rem = idx % (3 * C * 8);
+        const int third = rem / (C * 8), r = (rem / 8) % C, chunk = rem % 8;
+        ptr[u] = reinterpret_cast<uint4 *>(kq + p * SM::PANEL + (third * 64 + r) * 128 + chunk * 16);
+        keep[u] = r < (third == 2 ? Ln : L);
+        v[u] = keep[u] ? *ptr[u] : make_uint4(0, 0, 0, 0);
       }
-      *ptr = out;
+#pragma unroll
+      for (int u = 0; u < UNR; u++) {
+        uint4 out = make_uint4(0, 0, 0, 0);
+        if (keep[u]) {
+          const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&v[u]);
+          __half2 *h = reinterpret_cast<__half2 *>(&out);
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            const float2 f = __bfloat1622float2(b[i]);
+            h[i] = __floats2half2_rn(f.x, f.y);
+          }
+        }
+        *ptr[u] = out;
+      }
     }
   }
   fence_proxy_async();
@@ -547,7 +563,9 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     }
     named_bar(1 + wg, 128);
   }
-  if (t == 0) bulk_wait_all();
+  // the bulk stores must have read shared memory before the CTA exits; their
+  // global writes complete with the grid
+  if (t == 0) bulk_wait_read_all();
 
   // ---- tear-down ----
   fence_before_sync();

@@ -220,11 +220,44 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       if (lane == 0) mbar_arrive(bar(b));
     };
     bool nonfinite = false;
+    // ---- O_cc = scale gam Q_cc S_cc + AqkT_cc Y_cc (query lanes) ----
+    // Q_cc S_cc is in D3[cc & 1] (MMA3(cc + 1)), AqkT_cc Y_cc in
+    // D1[(cc + 1) & 1] (MMA1(cc + 1)); both stay until this thread's next
+    // SREADY arrival, which the products overwriting them wait for.  The
+    // output of chunk cc is written at the top of iteration cc + 2, while
+    // the tensor pipe runs the state products, so that its tensor-memory
+    // reads and global stores stay out of the window in which the key lanes
+    // form Y through shared memory.
+    auto output = [&](int cc, float sg) {
+      const int r = t - 64;
+      const int t0 = start + cc * C;
+      const int L = min(C, end - t0);
+      float qs[NH], d[NH];
+      lane_half(tD3 + (cc & 1) * NS, qs);
+      lane_half(tD1 + ((cc + 1) & 1) * NS, d);
+      if (r < L) {
+        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((long)(t0 + r) * a.HV + hv) * a.dv + col0 + c0;
+#pragma unroll
+        for (int ch = 0; ch < NH / 8; ch++) {
+          uint4 pk;
+          __nv_bfloat162 *pb = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            const int j = ch * 8 + 2 * i;
+            const float v0 = fmaf(sg, qs[j], d[j]);
+            const float v1 = fmaf(sg, qs[j + 1], d[j + 1]);
+            nonfinite |= !(isfinite(v0) && isfinite(v1));
+            pb[i] = __floats2bfloat162_rn(v0, v1);
+          }
+          *reinterpret_cast<uint4 *>(orow + ch * 8) = pk;
+        }
+      }
+    };
 
     if (nch > 0) {
       if (state_warp) write_state_image();
       signal(SM::B_SREADY);  // S_0
-      float dec_prev = 1.f, sgam_prev = 0.f;
+      float dec_prev = 1.f, sgam_prev = 0.f, sgam_prev2 = 0.f;
       for (int c = 0; c <= nch; c++) {
         // coefficients of chunk c (into registers, then the slot is handed back)
         float beta_r = 0.f, gam_r = 0.f, sgam_r = 0.f, dec_c = 0.f;
@@ -238,6 +271,18 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(SM::B_CFEMPTY + s));
         }
+        // this row of V_c into registers now, while the products of the
+        // previous chunk run: shared memory is quiet here, and busy with the
+        // state product's operand reads while Y_c is formed
+        uint4 vv[NH / 8];
+        if (key_warp && c < nch) {
+          mbar_wait(bar(SM::B_VFULL + (c & 1)), (c >> 1) & 1, abort_flag);
+          const unsigned char *vrow = sm + SM::kV + (c & 1) * SM::VI + t * 128;
+#pragma unroll
+          for (int ch = 0; ch < NH / 8; ch++)
+            vv[ch] = *reinterpret_cast<const uint4 *>(vrow + (((c0 / 8 + ch) ^ (t & 7)) << 4));
+        }
+        if (query_warp && c >= 2) output(c - 2, sgam_prev2);
         // ---- state: S_c = d_{c-1} S_{c-1} + P1_{c-1} Y_{c-1} ----
         if (c >= 1) {
           mbar_wait(bar(SM::B_MMA2), (c - 1) & 1, abort_flag);
@@ -267,12 +312,9 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
 #pragma unroll
             for (int i = 0; i < NH; i++) x[i] = fmaf(dec_prev, x[i], e[i]);
           }
-          mbar_wait(bar(SM::B_VFULL + (c & 1)), (c >> 1) & 1, abort_flag);
-          const unsigned char *vrow = sm + SM::kV + (c & 1) * SM::VI + t * 128;
 #pragma unroll
           for (int ch = 0; ch < NH / 8; ch++) {
-            const uint4 vv = *reinterpret_cast<const uint4 *>(vrow + (((c0 / 8 + ch) ^ (t & 7)) << 4));
-            const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(&vv);
+            const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(&vv[ch]);
             uint4 pk;
             __half2 *ph = reinterpret_cast<__half2 *>(&pk);
 #pragma unroll
@@ -285,35 +327,11 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
           }
           signal(SM::B_YREADY);
         }
-        if (query_warp && c >= 1) {
-          // ---- O_{c-1} = scale gam Q_{c-1} S_{c-1} + AqkT_{c-1} Y_{c-1} ----
-          const int r = t - 64;
-          const int t0 = start + (c - 1) * C;
-          const int L = min(C, end - t0);
-          float qs[NH], d[NH];
-          lane_half(d3, qs);
-          lane_half(d1, d);
-          if (r < L) {
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((long)(t0 + r) * a.HV + hv) * a.dv + col0 + c0;
-#pragma unroll
-            for (int ch = 0; ch < NH / 8; ch++) {
-              uint4 pk;
-              __nv_bfloat162 *pb = reinterpret_cast<__nv_bfloat162 *>(&pk);
-#pragma unroll
-              for (int i = 0; i < 4; i++) {
-                const int j = ch * 8 + 2 * i;
-                const float v0 = fmaf(sgam_prev, qs[j], d[j]);
-                const float v1 = fmaf(sgam_prev, qs[j + 1], d[j + 1]);
-                nonfinite |= !(isfinite(v0) && isfinite(v1));
-                pb[i] = __floats2bfloat162_rn(v0, v1);
-              }
-              *reinterpret_cast<uint4 *>(orow + ch * 8) = pk;
-            }
-          }
-        }
         dec_prev = dec_c;
+        sgam_prev2 = sgam_prev;
         sgam_prev = sgam_r;
       }
+      if (query_warp) output(nch - 1, sgam_prev2);
     }
 
     // ---- final state ----
