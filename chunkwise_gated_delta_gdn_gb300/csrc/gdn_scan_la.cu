@@ -26,7 +26,7 @@
 //    shared memory is the B operand of MMA3.  Lanes below C form Y (key rows),
 //    lanes 64..64+C-1 form O (query rows), lanes below dk update the state.
 //  * warp 8, one thread: issues every tensor-core product, the TMA loads of V
-//    (a two-deep ring) and the bulk copies of the prep images (three deep).
+//    (a three-deep ring) and the bulk copies of the prep images (three deep).
 //  * warp 9: gates and beta by cp.async, cumulative gates and the per-row
 //    coefficients (a four-deep ring).
 //  * warps 10-11: the [K_{c+1}; Q_c] operand (a two-deep ring): bulk copies of
@@ -61,12 +61,12 @@ static_assert(NS == 64, "one 128-byte swizzle atom per S / Y row");
 
 template <int C, int DK>
 struct LaSmem {
-  static constexpr int NKQ = 2, NP = 3, NCF = 4;
+  static constexpr int NKQ = 2, NP = 3, NCF = 4, NV = 3;
   static constexpr int KQ = (DK / 64) * 16384;  // [K_{c+1}; Q_c], K-major, 128 rows
   static constexpr int PI = kLaImageBytes;       // [P1; E; AqkT]
   static constexpr int SI = (DK / 8) * 1024;     // S, MN-major, dk K-rows
   static constexpr int YI = 8 * 1024;            // Y, MN-major, 64 K-rows
-  static constexpr int VI = C * 128;             // V slice, C rows x 64 bf16 (x2)
+  static constexpr int VI = C * 128;             // V slice, C rows x 64 bf16 (x NV)
   // per chunk: raw gates and beta (2C), then beta, gam, scale*gam (3C), decay
   static constexpr int CF = (5 * C + 4) * 4;
   static constexpr int kKQ = 0;
@@ -74,7 +74,7 @@ struct LaSmem {
   static constexpr int kS = kP + NP * PI;
   static constexpr int kY = kS + SI;
   static constexpr int kV = kY + YI;
-  static constexpr int kCf = kV + 2 * VI;
+  static constexpr int kCf = kV + NV * VI;
   static constexpr int kBar = kCf + NCF * CF;
   enum {
     B_KQFULL = 0,
@@ -89,8 +89,8 @@ struct LaSmem {
     B_MMA3 = B_MMA2 + 1,       // two, by chunk parity
     B_SREADY = B_MMA3 + 2,
     B_YREADY = B_SREADY + 1,
-    B_VFULL = B_YREADY + 1,    // two V buffers
-    NBAR = B_VFULL + 2
+    B_VFULL = B_YREADY + 1,    // NV V buffers
+    NBAR = B_VFULL + NV
   };
   static constexpr int kMisc = kBar + NBAR * 8;
   static constexpr int kUsed = kMisc + 16;
@@ -153,8 +153,8 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     for (int i = 0; i < 2; i++) {
       mbar_init(bar(SM::B_MMA1 + i), 1);
       mbar_init(bar(SM::B_MMA3 + i), 1);
-      mbar_init(bar(SM::B_VFULL + i), 1);
     }
+    for (int i = 0; i < SM::NV; i++) mbar_init(bar(SM::B_VFULL + i), 1);
     mbar_init(bar(SM::B_MMA2), 1);
     mbar_init(bar(SM::B_SREADY), kChain / 32);
     mbar_init(bar(SM::B_YREADY), kKeyWarps);
@@ -276,8 +276,8 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         // state product's operand reads while Y_c is formed
         uint4 vv[NH / 8];
         if (key_warp && c < nch) {
-          mbar_wait(bar(SM::B_VFULL + (c & 1)), (c >> 1) & 1, abort_flag);
-          const unsigned char *vrow = sm + SM::kV + (c & 1) * SM::VI + t * 128;
+          mbar_wait(bar(SM::B_VFULL + c % SM::NV), (c / SM::NV) & 1, abort_flag);
+          const unsigned char *vrow = sm + SM::kV + (c % SM::NV) * SM::VI + t * 128;
 #pragma unroll
           for (int ch = 0; ch < NH / 8; ch++)
             vv[ch] = *reinterpret_cast<const uint4 *>(vrow + (((c0 / 8 + ch) ^ (t & 7)) << 4));
@@ -351,10 +351,10 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     // =====================================================================
     if (lane == 0 && nch > 0) {
       const uint32_t sS = smem_addr(sm + SM::kS), sY = smem_addr(sm + SM::kY);
-      auto issue_v = [&](int cc) {  // V slice of chunk cc -> buffer cc & 1
-        const uint32_t b = bar(SM::B_VFULL + (cc & 1));
+      auto issue_v = [&](int cc) {  // V slice of chunk cc -> buffer cc % NV
+        const uint32_t b = bar(SM::B_VFULL + cc % SM::NV);
         mbar_arrive_expect_tx(b, SM::VI);
-        tma_load_3d(smem_addr(sm + SM::kV + (cc & 1) * SM::VI), &maps.v, col0, hv, start + cc * C, b);
+        tma_load_3d(smem_addr(sm + SM::kV + (cc % SM::NV) * SM::VI), &maps.v, col0, hv, start + cc * C, b);
       };
       auto issue_p = [&](int j) {  // prep image of chunk j -> slot j % NP
         const uint32_t b = bar(SM::B_PFULL + j % NP);
@@ -379,8 +379,7 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         mma_commit(bar(SM::B_KQEMPTY + s));
       };
 
-      issue_v(0);
-      if (nch > 1) issue_v(1);
+      for (int cc = 0; cc < SM::NV && cc < nch; cc++) issue_v(cc);
       issue_p(0);
       if (nch > 1) issue_p(1);
       mbar_wait(bar(SM::B_SREADY), 0, abort_flag);  // S_0 image
@@ -388,10 +387,6 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       mma3(1, 0);  // [K_1; Q_0] S_0 -> D3[0]
       for (int c = 1; c <= nch; c++) {
         mbar_wait(bar(SM::B_YREADY), (c - 1) & 1, abort_flag);  // Y_{c-1}, V_{c-1} consumed
-        if (c + 1 < nch) {
-          issue_v(c + 1);
-          issue_p(c + 1);
-        }
         const int ps = (c - 1) % NP;
         mbar_wait(bar(SM::B_PFULL + ps), ((c - 1) / NP) & 1, abort_flag);
         fence_after_sync();
@@ -409,6 +404,11 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
                   k0 > 0 ? 1u : 0u);
         }
         mma_commit(bar(SM::B_MMA1 + (c & 1)));
+        // loads for later chunks, after the products on the serial path: V of
+        // chunk c + 2 into the buffer V_{c-1} left, the prep image of chunk
+        // c + 1 into the slot that MMA2(c-1) and MMA1(c-1) have finished with
+        if (c + 2 < nch) issue_v(c + 2);
+        if (c + 1 < nch) issue_p(c + 1);
         if (c < nch) {
           mbar_wait(bar(SM::B_SREADY), c & 1, abort_flag);  // S_c image
           mma3(c + 1, c & 1);                               // [K_{c+1}; Q_c] S_c
