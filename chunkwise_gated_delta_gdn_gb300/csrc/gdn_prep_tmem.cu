@@ -2,15 +2,14 @@
 // the 5th-generation tensor cores.
 //
 // One CTA per (chunk slot, q/k head); its warpgroup (128 threads) takes the
-// group's value heads in turn (the kernel is written for NWG warpgroups taking
-// them in parallel; one measured faster, two CTAs sharing an SM).  The group
-// shares the key/query
-// tile and the next chunk's key tile: they arrive once by TMA (bf16, 128-byte
-// swizzle), are converted to fp16 in place, published for the scan kernel as
-// its [K_next; Q] operand image, and feed one Gram product for all value
-// heads:
+// group's value heads in turn.  Three CTAs share an SM: each holds 128
+// tensor-memory columns and about 75 KB of shared memory, and their
+// latency-bound phases overlap.  The group shares the key/query tile and the
+// next chunk's key tile: they arrive once by TMA (bf16, 128-byte swizzle), are
+// converted to fp16 in place, published for the scan kernel as its
+// [K_next; Q] operand image, and feed one Gram product for all value heads:
 //   G  = [K; Q] K^T          M = 128 (keys then queries), N = C, K = dk
-// Each warpgroup then, for its value head (gates and beta differ per head):
+// Then, for each value head in turn (gates and beta differ per head):
 //   A    = strict-lower(beta_r G_rs exp(b_r - b_s)), Aqk = lower(scale P_rs
 //          exp(b_r - b_s)) straight from its tensor-memory lanes; inside a
 //          32-row block the decay is one exp2 per entry, across blocks it is
@@ -26,9 +25,11 @@
 //                             of a sequence)
 // and writes them, each rounded once to fp16, as the 32 KB operand image of the
 // lookahead scan kernel (rows 0..127 = P1, 128..191 = E, 192..255 = AqkT;
-// K-major, 128-byte swizzle), staged in shared memory and stored with one bulk
-// copy.  The staged P1 rows double as E's B operand: a K-major image of P1's
-// dk rows is the MN-major layout of P1 read as a dk x C operand.  E lets the scan form
+// K-major, 128-byte swizzle), staged in shared memory over buffers that are
+// dead by then and stored with three bulk copies.  The three products take
+// turns in one 64-column tensor-memory buffer.  The staged P1 rows double as
+// E's B operand: a K-major image of P1's dk rows is the MN-major layout of P1
+// read as a dk x C operand.  E lets the scan form
 // the next chunk's K S from this chunk's Y without waiting for the state:
 //   K_next S_next = exp(b_last) K_next S + E Y.
 #include <cuda.h>
@@ -53,37 +54,43 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int C, int NWG>
+template <int C>
 struct PrepTmemSmem {
   static constexpr int LDT = C + 4;               // fp32 row stride of A^T / T^T
   // [K; Q; K_next], K-major, always two panels of 192 rows x 128 bytes
   static constexpr int PANEL = 192 * 128;
   static constexpr int KQ = 2 * PANEL;
-  // per warpgroup
-  static constexpr int WG_AQK = 0;                // Aqk, K-major, 64 rows (8 KB)
-  static constexpr int WG_IMG = 0;                // later: the 32 KB output image
-  static constexpr int WG_TI = 8 * 1024;          // T as a K-major B operand (8 KB)
-  static constexpr int WG_DTI = 16 * 1024;        // D T, likewise (8 KB)
-  static constexpr int WG_A = 24 * 1024;          // A^T -> T^T, fp32, row stride LDT
-  static constexpr int WG_R = WG_A + C * LDT * 4;  // 32 x 36 scratch (W tiles)
-  static constexpr int WG_G = WG_R + 32 * 36 * 4;  // cumulative gates (log2 units)
-  static constexpr int WG_BETA = WG_G + C * 4;
-  static constexpr int WG_DEC = WG_BETA + C * 4;
-  static constexpr int WG_BYTES = ((WG_DEC + C * 4 + 1023) / 1024) * 1024;
+  // Each panel's query rows (64..127) are free once the Gram has read them
+  // and the [K_next; Q] image has been stored: panel 0's hold the W scratch of
+  // the solve, then T as a K-major B operand, then the staged E rows; panel
+  // 1's hold D T.
+  static constexpr int QS0 = 64 * 128;
+  static constexpr int QS1 = PANEL + 64 * 128;
   static constexpr int kKQ = 0;
   static constexpr int kWG = KQ;
-  static constexpr int kBar = kWG + NWG * WG_BYTES;  // tma, gram, mma[NWG]
-  static constexpr int kMisc = kBar + (2 + NWG) * 8;
+  // per value head, reused in turn
+  static constexpr int WG_AQK = 0;                // Aqk, K-major, 64 rows (8 KB); then AqkT staged
+  static constexpr int WG_A = 8 * 1024;           // A^T -> T^T, fp32, row stride LDT; then P1 staged
+  static constexpr int A_BYTES = ((C * LDT * 4 > 16384 ? C * LDT * 4 : 16384) + 1023) / 1024 * 1024;
+  static constexpr int WG_G = WG_A + A_BYTES;     // cumulative gates (log2 units)
+  static constexpr int WG_BETA = WG_G + C * 4;
+  static constexpr int WG_DEC = WG_BETA + C * 4;
+  static constexpr int WG_WF = WG_DEC + C * 4;    // cross-block decay factors (32)
+  static constexpr int WG_BYTES = WG_WF + 32 * 4;
+  static constexpr int kBar = kWG + WG_BYTES;     // tma, gram, mma
+  static constexpr int kMisc = kBar + 3 * 8;
   static constexpr int kBytes = kMisc + 32 + 1024;
+  static_assert(kBar % 8 == 0, "mbarrier alignment");
+  static_assert(32 * 9 * 4 * 4 <= 8192, "W scratch in panel 0's query rows");
   static_assert(kBytes <= 232448, "shared memory of one CTA");
 };
 
-template <int C, int DK, int NWG>
-__global__ void __launch_bounds__(128 * NWG, NWG == 1 ? 2 : 1)
+template <int C, int DK>
+__global__ void __launch_bounds__(128, 3)
 gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
-  using SM = PrepTmemSmem<C, NWG>;
+  using SM = PrepTmemSmem<C>;
   constexpr int LDT = SM::LDT;
-  constexpr int NT = 128 * NWG;
+  constexpr int NT = 128;
   extern __shared__ unsigned char smem_raw[];
   // 1 KB-aligned base, as an offset into the shared array (the compiler then
   // knows every access below is to shared memory)
@@ -120,7 +127,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     if (valid) {
       mbar_init(bar_tma, 1);
       mbar_init(bar_gram, 1);
-      for (int w = 0; w < NWG; w++) mbar_init(bar_tma + 16 + 8 * w, 1);
+      mbar_init(bar_tma + 16, 1);
       mbar_fence_init();
     }
   }
@@ -128,8 +135,8 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   if (!meta[2]) return;  // unused slot: the scan never reads it
   const int t0 = meta[0], L = meta[1], Ln = meta[3];
 
-  // Gram (C columns) + per warpgroup P1 and Aqk T / E (2 x 64)
-  constexpr uint32_t kCols = NWG == 1 ? 256 : 512;
+  // Gram (C columns) at 0, then P1, Aqk T and E in turn at 64
+  constexpr uint32_t kCols = 128;
   if (warp == 0) tmem_alloc(smem_addr(tslot), kCols);
   if (C < 64) {  // zero the rows no TMA box covers
     for (int i = tid; i < SM::KQ / 16; i += NT) {
@@ -147,8 +154,8 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       if (Ln > 0) tma_load_3d(smem_addr(kq + p * SM::PANEL + 128 * 128), &maps.k, p * 64, hq, t0 + C, bar_tma);
     }
   }
-  // this warpgroup's first gates and beta, fetched while the tiles land
-  const int wg = warp >> 2, t = tid & 127;  // warpgroup, thread within it
+  // the first value head's gates and beta, fetched while the tiles land
+  const int t = tid;
   const int G = a.HV / a.H;
   float g_next = 0.f, b_next = 0.f;
   auto fetch = [&](int j) {
@@ -158,7 +165,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       b_next = __ldg(a.beta + row);
     }
   };
-  fetch(wg);
+  fetch(0);
   mbar_wait(bar_tma, 0, abort_flag);
   // bf16 -> fp16 in place; rows beyond each tile's tokens -> 0.  Six 16-byte
   // chunks per thread in flight at a time (the loop is shared-memory latency
@@ -225,26 +232,31 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     bulk_commit();
   }
 
-  // ---- per value head, one warpgroup each ----
-  unsigned char *ws = sm + SM::kWG + wg * SM::WG_BYTES;
+  // ---- per value head ----
+  unsigned char *ws = sm + SM::kWG;
   float *As = reinterpret_cast<float *>(ws + SM::WG_A);
-  float *Rs = reinterpret_cast<float *>(ws + SM::WG_R);
+  float *Rs = reinterpret_cast<float *>(sm + SM::QS0);  // W scratch of the solve
   float *Gs = reinterpret_cast<float *>(ws + SM::WG_G);
   float *Bs = reinterpret_cast<float *>(ws + SM::WG_BETA);
   float *Ds = reinterpret_cast<float *>(ws + SM::WG_DEC);
-  const uint32_t bar_mma = bar_tma + 16 + 8 * wg;
-  const uint32_t tP1 = tmem + 64 + 128 * wg, tAT = tP1 + 64;
+  const uint32_t bar_mma = bar_tma + 16;
+  const uint32_t tX = tmem + 64;  // P1, then Aqk T, then E
   const int wlane0 = (warp & 3) * 32;  // first tensor-memory lane of this warp
   int mma_uses = 0;  // completions of bar_mma so far
   bool first = true;
-  float *Wf = Rs;  // exp2(b_32 - b_s), s < 32 (the cross-block decay factors)
-  for (int j = wg; j < G; j += NWG) {
+  float *Wf = reinterpret_cast<float *>(ws + SM::WG_WF);  // exp2(b_32 - b_s), s < 32
+  for (int j = 0; j < G; j++) {
     const int hv = hq * G + j;
+    // the previous head's image stores must have read the buffers reused below
+    if (j > 0) {
+      if (t == 0) bulk_wait_read_all();
+      named_bar(1, 128);
+    }
     // gates (log2 units), beta, cumulative gates, end-of-chunk decays
     const float gv = g_next, bv = b_next;
     g_next = 0.f;
     b_next = 0.f;
-    fetch(j + NWG);
+    fetch(j + 1);
     bool positive = false;
     if (t < C) {
       positive = gv > 0.f;
@@ -252,7 +264,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       Bs[t] = bv;
     }
     if (__any_sync(0xffffffffu, positive) && lane == 0) atomicOr(a.flags, kFlagPositiveGate);
-    named_bar(1 + wg, 128);
+    named_bar(1, 128);
     if ((warp & 3) == 0) {
       float x0 = lane < C ? Gs[lane] : 0.f;
       float x1 = lane + 32 < C ? Gs[lane + 32] : 0.f;
@@ -268,19 +280,13 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       if (lane + 32 < C) { Gs[lane + 32] = x1; Ds[lane + 32] = ex2(blast - x1); }
       if (C > 32) Wf[lane] = ex2(__shfl_sync(0xffffffffu, x1, 0) - x0);
     }
-    named_bar(1 + wg, 128);
+    named_bar(1, 128);
     if (first) {
       mbar_wait(bar_gram, 0, abort_flag);
       fence_after_sync();
       first = false;
     }
 
-    // the previous head's image store must have read the staging area, which
-    // the writes below reuse
-    if (j != wg) {
-      if (t == 0) bulk_wait_read_all();
-      named_bar(1 + wg, 128);
-    }
     // ---- A (key lanes) and Aqk (query lanes) from the shared Gram ----
     // decay of column s for row r in 32-row block o: direct inside the block,
     // factored (ur * Wf[s]) for the earlier block.  A is stored transposed
@@ -345,9 +351,12 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       }
     }
     fence_before_sync();
-    named_bar(1 + wg, 128);
+    named_bar(1, 128);
 
     // ---- T = (I + A)^-1, transposed in place: As[j * LDT + r] = T[r][j] ----
+    // (the [K_next; Q] image store must have read the query rows that hold
+    // the W scratch from here on)
+    if (j == 0 && t == 0) bulk_wait_read_all();
     // (1) 16 x 16 diagonal blocks: warp w, lanes 0..15 = columns, rows in
     //     registers, forward substitution in fp32
     {
@@ -376,7 +385,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
         for (int m = 0; m < 4; m++)
           *reinterpret_cast<float4 *>(row + 4 * m) = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
       }
-      named_bar(1 + wg, 128);
+      named_bar(1, 128);
       // (2) 32 x 32 blocks from their 16 x 16 halves: T10 = -T11 (A10 T00),
       //     one warp per (32-block, 8-column tile); split-tf32 tensor-core
       //     products (fp32-class accuracy), W staged in the warp's rows of Rs
@@ -395,7 +404,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
         Wt2[gq * 9 + 2 * tq] = w[0]; Wt2[gq * 9 + 2 * tq + 1] = w[1];
         Wt2[(gq + 8) * 9 + 2 * tq] = w[2]; Wt2[(gq + 8) * 9 + 2 * tq + 1] = w[3];
       }
-      named_bar(1 + wg, 128);  // both warps of a block have read A10 before T10 overwrites it
+      named_bar(1, 128);  // both warps of a block have read A10 before T10 overwrites it
       if (act2) {
         float u[4] = {0.f, 0.f, 0.f, 0.f}, uc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -410,7 +419,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
         As[(ob + n2 + 2 * tq) * LDT + ob + 24 + gq] = -u[2];
         As[(ob + n2 + 2 * tq + 1) * LDT + ob + 24 + gq] = -u[3];
       }
-      named_bar(1 + wg, 128);
+      named_bar(1, 128);
       if constexpr (C == 64) {
         // (3) the 64 x 64 inverse from its 32 x 32 halves: T10 = -T11 (A10 T00),
         //     warp w owns columns 8w .. 8w+7 of W and of T10
@@ -432,7 +441,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
           Wt[(16 * mt + gq) * 9 + 2 * tq] = w[mt][0]; Wt[(16 * mt + gq) * 9 + 2 * tq + 1] = w[mt][1];
           Wt[(16 * mt + gq + 8) * 9 + 2 * tq] = w[mt][2]; Wt[(16 * mt + gq + 8) * 9 + 2 * tq + 1] = w[mt][3];
         }
-        named_bar(1 + wg, 128);  // every warp has read A10 before T10 overwrites it
+        named_bar(1, 128);  // every warp has read A10 before T10 overwrites it
         float u[2][4] = {}, uc[2][4] = {};
 #pragma unroll
         for (int k0 = 0; k0 < 32; k0 += 8)
@@ -452,7 +461,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
           As[(n0 + 2 * tq) * LDT + 40 + 16 * mt + gq] = -u[mt][2];
           As[(n0 + 2 * tq + 1) * LDT + 40 + 16 * mt + gq] = -u[mt][3];
         }
-        named_bar(1 + wg, 128);
+        named_bar(1, 128);
       }
     }
 
@@ -473,40 +482,18 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
         ht[2] = __floats2half2_rn(t1v.x, t1v.y); ht[3] = __floats2half2_rn(t1v.z, t1v.w);
         hd[0] = __floats2half2_rn(d0.x * t0v.x, d0.y * t0v.y); hd[1] = __floats2half2_rn(d0.z * t0v.z, d0.w * t0v.w);
         hd[2] = __floats2half2_rn(d1.x * t1v.x, d1.y * t1v.y); hd[3] = __floats2half2_rn(d1.z * t1v.z, d1.w * t1v.w);
-        *reinterpret_cast<uint4 *>(ws + SM::WG_TI + kmajor_off(j, ch * 8, 64)) = pt;
-        *reinterpret_cast<uint4 *>(ws + SM::WG_DTI + kmajor_off(j, ch * 8, 64)) = pd;
+        *reinterpret_cast<uint4 *>(sm + SM::QS0 + kmajor_off(j, ch * 8, 64)) = pt;
+        *reinterpret_cast<uint4 *>(sm + SM::QS1 + kmajor_off(j, ch * 8, 64)) = pd;
       }
     }
     fence_proxy_async();
     fence_before_sync();
-    named_bar(1 + wg, 128);
+    named_bar(1, 128);
     fence_after_sync();
 
-    // ---- P1 = K^T (D T), AqkT = Aqk T ----
-    if (t == 0) {
-      const uint32_t sKQ = smem_addr(kq), sAqk = smem_addr(ws + SM::WG_AQK);
-      const uint32_t sT = smem_addr(ws + SM::WG_TI), sDT = smem_addr(ws + SM::WG_DTI);
-      constexpr uint32_t idP = idesc_f16(128, C, 1, 0);  // A MN-major: keys read as K^T
-      constexpr uint32_t idQ = idesc_f16(128, C, 0, 0);
-#pragma unroll
-      for (int k0 = 0; k0 < C; k0 += 16) {
-        mma_f16(tP1, make_desc(sKQ + k0 * 128, SM::PANEL, 1024),
-                make_desc(sDT + k0 * 2, 16, 1024), idP, k0 > 0 ? 1u : 0u);
-      }
-#pragma unroll
-      for (int k0 = 0; k0 < C; k0 += 16) {
-        mma_f16(tAT, make_desc(sAqk + k0 * 2, 16, 1024),
-                make_desc(sT + k0 * 2, 16, 1024), idQ, k0 > 0 ? 1u : 0u);
-      }
-      mma_commit(bar_mma);
-    }
-    mbar_wait(bar_mma, mma_uses++ & 1, abort_flag);
-    fence_after_sync();
-
-    // ---- the image, staged in shared memory over the dead per-head buffers ----
-    unsigned char *img = ws + SM::WG_IMG;
-    // image row `row` <- this lane's row at `taddr` (zeros when !have)
-    auto put_row = [&](int row, uint32_t taddr, bool have) {
+    // this lane's row at `taddr` -> row `row` of a 64-column K-major fp16
+    // image at `dst` (zeros when !have)
+    auto put_row = [&](unsigned char *dst, int row, uint32_t taddr, bool have) {
 #pragma unroll
       for (int h = 0; h < 2; h++) {  // 32 columns at a time
         uint32_t v[32];
@@ -525,26 +512,61 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
             const float f1 = load ? __uint_as_float(v[ch * 8 + 2 * i + 1]) : 0.f;
             hh[i] = __floats2half2_rn(f0, f1);
           }
-          *reinterpret_cast<uint4 *>(img + kmajor_off(row, 32 * h + ch * 8, kLaImageRows)) = pk;
+          *reinterpret_cast<uint4 *>(dst + kmajor_off(row, 32 * h + ch * 8, 64)) = pk;
         }
       }
     };
-    if (t < 64) put_row(192 + t, tAT + lane_base, wlane0 < C);
-    put_row(t, tP1 + lane_base, wlane0 < DK);
+    // staging of the image, over buffers dead by then: P1 (rows 0..127) over
+    // A^T, E (rows 128..191) over the T image, Aqk T (rows 192..255) over Aqk
+    unsigned char *stP1 = ws + SM::WG_A, *stE = sm + SM::QS0, *stAT = ws + SM::WG_AQK;
+    const uint32_t sKQ = smem_addr(kq);
+
+    // ---- P1 = K^T (D T) ----
+    if (t == 0) {
+      const uint32_t sDT = smem_addr(sm + SM::QS1);
+      constexpr uint32_t idP = idesc_f16(128, C, 1, 0);  // A MN-major: keys read as K^T
+#pragma unroll
+      for (int k0 = 0; k0 < C; k0 += 16) {
+        mma_f16(tX, make_desc(sKQ + k0 * 128, SM::PANEL, 1024),
+                make_desc(sDT + k0 * 2, 16, 1024), idP, k0 > 0 ? 1u : 0u);
+      }
+      mma_commit(bar_mma);
+    }
+    mbar_wait(bar_mma, mma_uses++ & 1, abort_flag);
+    fence_after_sync();
+    put_row(stP1, t, tX + lane_base, wlane0 < DK);
     fence_proxy_async();
     fence_before_sync();
-    named_bar(1 + wg, 128);
+    named_bar(1, 128);
     fence_after_sync();
 
-    // ---- E = K_next P1 (M = 128 rows from the next-key tile, N = C, K = dk),
-    //      into the Aqk T columns that were just read out ----
+    // ---- AqkT = Aqk T ----
+    if (t == 0) {
+      const uint32_t sAqk = smem_addr(ws + SM::WG_AQK), sT = smem_addr(sm + SM::QS0);
+      constexpr uint32_t idQ = idesc_f16(128, C, 0, 0);
+#pragma unroll
+      for (int k0 = 0; k0 < C; k0 += 16) {
+        mma_f16(tX, make_desc(sAqk + k0 * 2, 16, 1024),
+                make_desc(sT + k0 * 2, 16, 1024), idQ, k0 > 0 ? 1u : 0u);
+      }
+      mma_commit(bar_mma);
+    }
+    mbar_wait(bar_mma, mma_uses++ & 1, abort_flag);
+    fence_after_sync();
+    if (t < 64) put_row(stAT, t, tX + lane_base, wlane0 < C);
+    fence_proxy_async();
+    fence_before_sync();
+    named_bar(1, 128);
+    fence_after_sync();
+
+    // ---- E = K_next P1 (M = 128 rows from the next-key tile, N = C, K = dk) ----
     if (Ln > 0) {
       if (t == 0) {
-        const uint32_t sKn = smem_addr(kq) + 128 * 128, sP1 = smem_addr(img);
+        const uint32_t sKn = sKQ + 128 * 128, sP1 = smem_addr(stP1);
         constexpr uint32_t idE = idesc_f16(128, C, 0, 1);
 #pragma unroll
         for (int k0 = 0; k0 < DK; k0 += 16) {
-          mma_f16(tAT, make_desc(sKn + (k0 >> 6) * SM::PANEL + (k0 & 63) * 2, 16, 1024),
+          mma_f16(tX, make_desc(sKn + (k0 >> 6) * SM::PANEL + (k0 & 63) * 2, 16, 1024),
                   make_desc(sP1 + (k0 >> 4) * 2048, (DK / 8) * 1024, 1024), idE, k0 > 0 ? 1u : 0u);
         }
         mma_commit(bar_mma);
@@ -552,16 +574,18 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       mbar_wait(bar_mma, mma_uses++ & 1, abort_flag);
       fence_after_sync();
     }
-    if (t < 64) put_row(128 + t, tAT + lane_base, Ln > 0 && wlane0 < C);
+    if (t < 64) put_row(stE, t, tX + lane_base, Ln > 0 && wlane0 < C);
     fence_proxy_async();
     fence_before_sync();
-    named_bar(1 + wg, 128);
+    named_bar(1, 128);
+    fence_after_sync();
     if (t == 0) {
-      bulk_s2g(reinterpret_cast<unsigned char *>(a.tiles) + ((size_t)slot * a.HV + hv) * kLaImageBytes,
-               smem_addr(img), kLaImageBytes);
+      unsigned char *dst = reinterpret_cast<unsigned char *>(a.tiles) + ((size_t)slot * a.HV + hv) * kLaImageBytes;
+      bulk_s2g(dst, smem_addr(stP1), 128 * 128);
+      bulk_s2g(dst + 128 * 128, smem_addr(stE), 64 * 128);
+      bulk_s2g(dst + 192 * 128, smem_addr(stAT), 64 * 128);
       bulk_commit();
     }
-    named_bar(1 + wg, 128);
   }
   // the bulk stores must have read shared memory before the CTA exits; their
   // global writes complete with the grid
@@ -575,34 +599,28 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   if (*abort_flag && tid == 0) atomicOr(a.flags, kFlagTimeout);
 }
 
-template <int C, int DK, int NWG>
+template <int C, int DK>
 cudaError_t launch_one(const PrepArgs &a, const ScanMaps &maps, cudaStream_t stream) {
-  using SM = PrepTmemSmem<C, NWG>;
-  auto kern = gdn_prep_tmem_kernel<C, DK, NWG>;
+  using SM = PrepTmemSmem<C>;
+  auto kern = gdn_prep_tmem_kernel<C, DK>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
   if (err != cudaSuccess) return err;
-  kern<<<dim3(a.n_slots, a.H), 128 * NWG, SM::kBytes, stream>>>(a, maps);
+  // three CTAs per SM need the largest shared-memory carve-out
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (err != cudaSuccess) return err;
+  kern<<<dim3(a.n_slots, a.H), 128, SM::kBytes, stream>>>(a, maps);
   return cudaGetLastError();
-}
-
-template <int C, int DK>
-cudaError_t dispatch_wg(const PrepArgs &a, const ScanMaps &maps, cudaStream_t s) {
-  // one warpgroup walking the group's value heads in turn: about 97 KB of
-  // shared memory and 256 tensor-memory columns, so two CTAs share an SM and
-  // overlap each other's latency-bound phases (measured faster than one
-  // warpgroup per value head at one CTA per SM)
-  return launch_one<C, DK, 1>(a, maps, s);
 }
 
 }  // namespace
 
 cudaError_t launch_prep_tmem(const PrepArgs &a, const ScanMaps &maps, int chunk, int dk,
                              cudaStream_t stream) {
-  if (chunk == 64 && dk == 128) return dispatch_wg<64, 128>(a, maps, stream);
-  if (chunk == 64 && dk == 64) return dispatch_wg<64, 64>(a, maps, stream);
-  if (chunk == 32 && dk == 128) return dispatch_wg<32, 128>(a, maps, stream);
-  if (chunk == 32 && dk == 64) return dispatch_wg<32, 64>(a, maps, stream);
+  if (chunk == 64 && dk == 128) return launch_one<64, 128>(a, maps, stream);
+  if (chunk == 64 && dk == 64) return launch_one<64, 64>(a, maps, stream);
+  if (chunk == 32 && dk == 128) return launch_one<32, 128>(a, maps, stream);
+  if (chunk == 32 && dk == 64) return launch_one<32, 64>(a, maps, stream);
   return cudaErrorInvalidValue;
 }
 
