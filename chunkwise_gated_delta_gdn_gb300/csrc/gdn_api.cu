@@ -350,6 +350,95 @@ gdn_status gdn_recurrent_fwd(const void *q, const void *k, const void *v, const 
   return GDN_OK;
 }
 
+gdn_status gdn_causal_conv1d_fwd(const void *x, const float *w, const float *bias,
+                                 const float *h0, void *y, float *hT,
+                                 const int32_t *cu_seqlens, int n_seqs, int B, int T, int D,
+                                 int width, int activation, int dtype, uint32_t *flags,
+                                 gdn_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (B <= 0 || T < 0 || D <= 0 || width <= 0) return GDN_ERR_INVALID_ARG;
+  if (activation != GDN_ACT_NONE && activation != GDN_ACT_SILU) return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  const bool packed = cu_seqlens != nullptr;
+  int n_states;
+  if (packed) {
+    if (B != 1 || n_seqs <= 0) return GDN_ERR_INVALID_ARG;
+    n_states = n_seqs;
+  } else {
+    if (n_seqs != 0 && n_seqs != B) return GDN_ERR_INVALID_ARG;
+    n_states = B;
+  }
+  if (width > 4 || D % 8 != 0) return GDN_ERR_UNSUPPORTED;
+  const long Ttot = (long)B * T;
+  if (Ttot > INT32_MAX || (long)n_states * D > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+  if (!w || (Ttot > 0 && (!x || !y))) return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {x, w, bias, h0, y, hT, cu_seqlens};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+  if (flags && (reinterpret_cast<uintptr_t>(flags) & 3u) != 0) return GDN_ERR_INVALID_ARG;
+  const size_t es = dtype == GDN_BF16 ? 2 : 4;
+  const size_t n_x = (size_t)Ttot * D * es, n_w = (size_t)D * width * 4, n_b = (size_t)D * 4;
+  const size_t n_h = (size_t)n_states * D * (width - 1) * 4;
+  const size_t n_cu = packed ? ((size_t)n_seqs + 1) * 4 : 0;
+  if (hT != h0 && overlap(hT, n_h, h0, n_h)) return GDN_ERR_INVALID_ARG;
+  const void *ins[] = {x, w, bias, cu_seqlens};
+  const size_t in_n[] = {n_x, n_w, n_b, n_cu};
+  for (int i = 0; i < 4; i++)
+    if (overlap(y, n_x, ins[i], in_n[i]) || overlap(hT, n_h, ins[i], in_n[i]) ||
+        overlap(flags, 4, ins[i], in_n[i]))
+      return GDN_ERR_INVALID_ARG;
+  if (overlap(y, n_x, h0, n_h) || overlap(y, n_x, hT, n_h) || overlap(flags, 4, y, n_x) ||
+      overlap(flags, 4, h0, n_h) || overlap(flags, 4, hT, n_h))
+    return GDN_ERR_INVALID_ARG;
+
+  if (flags && cudaMemsetAsync(flags, 0, sizeof(uint32_t), stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  gdn::ConvArgs ca;
+  ca.x = x; ca.w = w; ca.bias = bias; ca.h0 = h0; ca.y = y; ca.hT = hT;
+  ca.seq.cu = cu_seqlens;
+  ca.seq.n_seqs = n_states;
+  ca.seq.T = T;
+  ca.seq.Ttot = (int)Ttot;
+  ca.D = D;
+  ca.flags = flags;
+  if (gdn::launch_conv1d(ca, width, activation, dtype, stream) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+static gdn_status rownorm(int kind, const void *x, const void *z, const float *weight, void *y,
+                          int64_t rows, int dim, float eps, int dtype, gdn_stream_t stream_) {
+  if (rows < 0 || dim <= 0 || !(eps >= 0.f) || !std::isfinite(eps)) return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (!(dim == 64 || dim == 128 || dim == 256)) return GDN_ERR_UNSUPPORTED;
+  if (rows > 0 && (!x || !y)) return GDN_ERR_INVALID_ARG;
+  if (kind == 1 && !weight) return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {x, z, weight, y};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+  const size_t es = dtype == GDN_BF16 ? 2 : 4;
+  const size_t n = (size_t)rows * dim * es;
+  // y may be x itself (in place); any other overlap is refused
+  if (y != x && overlap(y, n, x, n)) return GDN_ERR_INVALID_ARG;
+  if (overlap(y, n, z, n) || overlap(y, n, weight, (size_t)dim * 4)) return GDN_ERR_INVALID_ARG;
+  gdn::RowNormArgs ra;
+  ra.x = x; ra.z = z; ra.weight = weight; ra.y = y; ra.rows = (long)rows; ra.eps = eps;
+  if (gdn::launch_rownorm(ra, dim, kind, dtype, reinterpret_cast<cudaStream_t>(stream_)) !=
+      cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+gdn_status gdn_l2norm_fwd(const void *x, void *y, int64_t rows, int dim, float eps, int dtype,
+                          gdn_stream_t stream) {
+  return rownorm(0, x, nullptr, nullptr, y, rows, dim, eps, dtype, stream);
+}
+
+gdn_status gdn_rmsnorm_gated_fwd(const void *x, const void *z, const float *weight, void *y,
+                                 int64_t rows, int dim, float eps, int dtype,
+                                 gdn_stream_t stream) {
+  return rownorm(1, x, z, weight, y, rows, dim, eps, dtype, stream);
+}
+
 gdn_status gdn_read_device_flags(const void *workspace, uint32_t *flags_out,
                                  gdn_stream_t stream_) {
   if (!workspace || !flags_out) return GDN_ERR_INVALID_ARG;

@@ -81,6 +81,24 @@ struct RecurrentArgs {
   uint32_t *flags;  // device status word, or nullptr
 };
 
+// The operations either side of the recurrence (gdn_prepost.cu).
+struct ConvArgs {
+  const void *x;
+  const float *w, *bias, *h0;  // w [D][W]; bias [D] or nullptr; h0 [N][D][W-1] or nullptr
+  void *y;
+  float *hT;                   // [N][D][W-1] or nullptr; may be h0 itself
+  SeqInfo seq;
+  int D;
+  uint32_t *flags;             // device status word, or nullptr
+};
+struct RowNormArgs {
+  const void *x, *z;           // z: gate rows (gated RMS norm only), or nullptr
+  const float *weight;         // [dim] (gated RMS norm only)
+  void *y;
+  long rows;
+  float eps;
+};
+
 // Status-word bits (same values as GDN_FLAG_* in include/gdn.h).
 constexpr uint32_t kFlagPositiveGate = 1u << 0;
 constexpr uint32_t kFlagNonfinite = 1u << 1;
@@ -113,6 +131,13 @@ cudaError_t launch_scan_tc(const ScanArgs &a, const ScanMaps &maps, int chunk, i
 cudaError_t launch_prep_tmem(const PrepArgs &a, const ScanMaps &maps, int chunk, int dk,
                              cudaStream_t stream);
 cudaError_t launch_scan_la(const ScanArgs &a, const ScanMaps &maps, int chunk, int dk,
+                           cudaStream_t stream);
+// causal depthwise convolution (width 1..4, D a multiple of 8; activation 0 =
+// none, 1 = SiLU) and the row norms (kind 0 = L2, 1 = gated RMS; dim 64, 128
+// or 256)
+cudaError_t launch_conv1d(const ConvArgs &a, int width, int activation, int dtype,
+                          cudaStream_t stream);
+cudaError_t launch_rownorm(const RowNormArgs &a, int dim, int kind, int dtype,
                            cudaStream_t stream);
 // token-serial form; dv a multiple of 32
 cudaError_t launch_recurrent(const RecurrentArgs &a, int dk, int dtype, int gate,

@@ -29,6 +29,9 @@ GDN_GATE_PER_KEY = 1
 GDN_F32 = 0
 GDN_BF16 = 1
 
+GDN_ACT_NONE = 0
+GDN_ACT_SILU = 1
+
 GDN_FLAG_POSITIVE_GATE = 1 << 0
 GDN_FLAG_NONFINITE = 1 << 1
 GDN_FLAG_BAD_SEQLENS = 1 << 2
@@ -37,7 +40,8 @@ GDN_FLAG_TIMEOUT = 1 << 3
 # every symbol include/gdn.h declares
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_chunk_fwd_workspace_bytes",
             "gdn_chunk_fwd", "gdn_chunk_fwd_prep", "gdn_chunk_fwd_scan",
-            "gdn_chunk_fwd_noalloc", "gdn_recurrent_fwd", "gdn_read_device_flags")
+            "gdn_chunk_fwd_noalloc", "gdn_recurrent_fwd", "gdn_causal_conv1d_fwd",
+            "gdn_l2norm_fwd", "gdn_rmsnorm_gated_fwd", "gdn_read_device_flags")
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +88,14 @@ def load(path: Optional[str] = None):
         lib.gdn_recurrent_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                           i32, i32, i32, i32, f32, i32, i32, vp, vp]
         lib.gdn_recurrent_fwd.restype = i32
+        lib.gdn_causal_conv1d_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                              i32, i32, i32, vp, vp]
+        lib.gdn_causal_conv1d_fwd.restype = i32
+        i64 = ctypes.c_int64
+        lib.gdn_l2norm_fwd.argtypes = [vp, vp, i64, i32, f32, i32, vp]
+        lib.gdn_l2norm_fwd.restype = i32
+        lib.gdn_rmsnorm_gated_fwd.argtypes = [vp, vp, vp, vp, i64, i32, f32, i32, vp]
+        lib.gdn_rmsnorm_gated_fwd.restype = i32
         lib.gdn_read_device_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gdn_read_device_flags.restype = i32
         _lib = lib
@@ -258,6 +270,94 @@ def gdn_recurrent_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torc
     if status != GDN_OK:
         raise GdnError(status, "gdn_recurrent_fwd")
     return o, hT
+
+
+def _check(t, name, dev):
+    if t is not None and (t.device != dev or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous tensor on {dev}")
+
+
+def gdn_causal_conv1d_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                          h0: Optional[torch.Tensor] = None, *, activation: int = GDN_ACT_NONE,
+                          cu_seqlens: Optional[torch.Tensor] = None,
+                          y: Optional[torch.Tensor] = None, hT: Optional[torch.Tensor] = None,
+                          output_final_state: bool = True,
+                          flags: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None
+                          ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Causal depthwise convolution with history; returns ``(y, hT)``.
+
+    x ``[B, T, D]`` (bf16 or fp32; packed ``[1, Ttot, D]`` with cu_seqlens);
+    w ``[D, W]`` fp32; bias ``[D]`` fp32 or None; h0 / hT ``[N, D, W-1]`` fp32
+    (``hT=h0`` updates the history in place).
+    """
+    lib = load()
+    B, T, D = x.shape
+    W = w.shape[1]
+    dev = x.device
+    for name, t in (("x", x), ("w", w), ("bias", bias), ("h0", h0), ("cu_seqlens", cu_seqlens),
+                    ("y", y), ("hT", hT), ("flags", flags)):
+        _check(t, name, dev)
+    for name, t in (("w", w), ("bias", bias), ("h0", h0)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    n_seqs = int(cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    if y is None:
+        y = torch.empty_like(x)
+    if hT is None and output_final_state:
+        hT = torch.empty((n_seqs, D, W - 1), dtype=torch.float32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    status = lib.gdn_causal_conv1d_fwd(
+        _ptr(x), _ptr(w), _ptr(bias), _ptr(h0), _ptr(y), _ptr(hT), _ptr(cu_seqlens), n_seqs, B,
+        T, D, W, int(activation), _dtype_code(x.dtype), _ptr(flags),
+        ctypes.c_void_p(stream.cuda_stream))
+    if status != GDN_OK:
+        raise GdnError(status, "gdn_causal_conv1d_fwd")
+    return y, hT
+
+
+def gdn_l2norm_fwd(x: torch.Tensor, *, eps: float = 1e-6, y: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Rows of x (last axis) divided by sqrt(sum of squares + eps)."""
+    lib = load()
+    _check(x, "x", x.device)
+    _check(y, "y", x.device)
+    if y is None:
+        y = torch.empty_like(x)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    dim = x.shape[-1]
+    status = lib.gdn_l2norm_fwd(_ptr(x), _ptr(y), x.numel() // max(dim, 1), dim, float(eps),
+                                _dtype_code(x.dtype), ctypes.c_void_p(stream.cuda_stream))
+    if status != GDN_OK:
+        raise GdnError(status, "gdn_l2norm_fwd")
+    return y
+
+
+def gdn_rmsnorm_gated_fwd(x: torch.Tensor, weight: torch.Tensor, z: Optional[torch.Tensor] = None,
+                          *, eps: float = 1e-6, y: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Rows of x scaled to unit RMS, times weight (fp32), times silu(z)."""
+    lib = load()
+    dev = x.device
+    for name, t in (("x", x), ("weight", weight), ("z", z), ("y", y)):
+        _check(t, name, dev)
+    if weight.dtype != torch.float32:
+        raise TypeError("weight must be float32")
+    if z is not None and (z.shape != x.shape or z.dtype != x.dtype):
+        raise ValueError("z must match x in shape and dtype")
+    if y is None:
+        y = torch.empty_like(x)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    dim = x.shape[-1]
+    status = lib.gdn_rmsnorm_gated_fwd(_ptr(x), _ptr(z), _ptr(weight), _ptr(y),
+                                       x.numel() // max(dim, 1), dim, float(eps),
+                                       _dtype_code(x.dtype), ctypes.c_void_p(stream.cuda_stream))
+    if status != GDN_OK:
+        raise GdnError(status, "gdn_rmsnorm_gated_fwd")
+    return y
 
 
 def gdn_read_device_flags(workspace: torch.Tensor,

@@ -77,6 +77,11 @@ typedef enum gdn_dtype {
   GDN_BF16 = 1  /* q, k, v, o are bfloat16 */
 } gdn_dtype;
 
+typedef enum gdn_activation {
+  GDN_ACT_NONE = 0,  /* identity */
+  GDN_ACT_SILU = 1   /* x * sigmoid(x) */
+} gdn_activation;
+
 /* Bits of the device status word kept in the first bytes of the workspace. */
 enum {
   GDN_FLAG_POSITIVE_GATE = 1u << 0, /* some log-gate g > 0 (a decay above 1) */
@@ -227,6 +232,54 @@ GDN_API gdn_status gdn_recurrent_fwd(const void *q, const void *k, const void *v
                                      int n_seqs, int B, int T, int H, int HV, int dk,
                                      int dv, float scale, int gate_mode, int dtype,
                                      uint32_t *flags, gdn_stream_t stream);
+
+/*
+ * Operations either side of the recurrence.  The pages keep them out of the
+ * recurrence's own contract (logismos issue #46, "Remaining work": gating,
+ * packing and convolution compose separately from the generic operation), so
+ * they are entry points of their own, each one memory-bound kernel.
+ *
+ * gdn_causal_conv1d_fwd -- causal depthwise convolution over time with a
+ * raw-input history (issue #46, "Verified implementation boundary": the
+ * staged causal convolution step keeps a channel-major, oldest-to-newest raw
+ * history, writes the next history and the output to separate buffers, and
+ * has no history for width 1).  For each sequence, channel c and
+ * ext = [history of c; x of c]:
+ *     y[t, c] = act(bias[c] + sum_{j < W} w[c, j] * ext[t + j])
+ * (w[c, W-1] weighs the current input), and the next history is the last
+ * W - 1 entries of ext, so a sequence shorter than W - 1 keeps part of the
+ * old one.  Layouts: x, y [B, T, D] (or packed [1, Ttot, D] with cu_seqlens)
+ * in dtype; w [D, W], bias [D] (or NULL), h0, hT [N, D, W-1] fp32 (h0 NULL =
+ * zeros; hT NULL = not written; hT may be h0 itself).  y must not overlap x.
+ * Supported: W in 1..4, D a multiple of 8, dtype F32 or BF16, activation
+ * GDN_ACT_NONE or GDN_ACT_SILU.  flags: as for gdn_recurrent_fwd
+ * (GDN_FLAG_BAD_SEQLENS).  With T == 1 this is the one-token decode step.
+ */
+GDN_API gdn_status gdn_causal_conv1d_fwd(const void *x, const float *w, const float *bias,
+                                         const float *h0, void *y, float *hT,
+                                         const int32_t *cu_seqlens, int n_seqs, int B, int T,
+                                         int D, int width, int activation, int dtype,
+                                         uint32_t *flags, gdn_stream_t stream);
+
+/*
+ * gdn_l2norm_fwd -- rows of x ([rows, dim], dtype) divided by
+ * sqrt(sum of squares + eps): the unit-norm queries and keys the recurrence
+ * expects.  y may be x itself.  dim in {64, 128, 256}.
+ */
+GDN_API gdn_status gdn_l2norm_fwd(const void *x, void *y, int64_t rows, int dim, float eps,
+                                  int dtype, gdn_stream_t stream);
+
+/*
+ * gdn_rmsnorm_gated_fwd -- the output norm that follows the recurrence
+ * (stratat pull #1296, re-base notes; the pages print no formula, and this is
+ * the plain reading): per row of x ([rows, dim], dtype)
+ *     y = x / sqrt(mean(x^2) + eps) * weight * silu(z)     (z NULL: no gate)
+ * with weight [dim] fp32 and z [rows, dim] in dtype.  y may be x itself.
+ * dim in {64, 128, 256}.
+ */
+GDN_API gdn_status gdn_rmsnorm_gated_fwd(const void *x, const void *z, const float *weight,
+                                         void *y, int64_t rows, int dim, float eps, int dtype,
+                                         gdn_stream_t stream);
 
 /*
  * Copy the device status word of `workspace` to *flags_out (host pointer)

@@ -165,3 +165,58 @@ def call_rec(lib, **kw):
 ])
 def test_recurrent_refusals(lib, kw, status):
     assert call_rec(lib, **kw) == status
+
+
+def call_conv(lib, **kw):
+    a = dict(x=addr(0), w=addr(1), bias=addr(2), h0=addr(3), y=addr(4), hT=addr(5), cu=None,
+             n_seqs=1, B=1, T=16, D=256, width=4, act=1, dtype=1, flags=addr(8))
+    a.update(kw)
+    return lib.gdn_causal_conv1d_fwd(a["x"], a["w"], a["bias"], a["h0"], a["y"], a["hT"],
+                                     a["cu"], a["n_seqs"], a["B"], a["T"], a["D"], a["width"],
+                                     a["act"], a["dtype"], a["flags"], None)
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(x=None), gdn.GDN_ERR_INVALID_ARG),
+    (dict(w=None), gdn.GDN_ERR_INVALID_ARG),
+    (dict(B=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(width=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(act=2), gdn.GDN_ERR_INVALID_ARG),
+    (dict(dtype=5), gdn.GDN_ERR_INVALID_ARG),
+    (dict(width=5), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(D=252), gdn.GDN_ERR_UNSUPPORTED),             # not a multiple of 8
+    (dict(y=addr(0)), gdn.GDN_ERR_INVALID_ARG),          # y aliases x
+    (dict(hT=ctypes.c_void_p(BASE + 3 * STRIDE + 64)), gdn.GDN_ERR_INVALID_ARG),  # partial overlap
+    (dict(x=ctypes.c_void_p(BASE + 4)), gdn.GDN_ERR_INVALID_ARG),
+    (dict(cu=addr(9), B=2, n_seqs=2), gdn.GDN_ERR_INVALID_ARG),
+])
+def test_conv_refusals(lib, kw, status):
+    assert call_conv(lib, **kw) == status
+
+
+@pytest.mark.parametrize("entry", ["l2", "rms"])
+@pytest.mark.parametrize("kw, status", [
+    (dict(rows=-1), gdn.GDN_ERR_INVALID_ARG),
+    (dict(dim=96), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dim=512), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(eps=float("nan")), gdn.GDN_ERR_INVALID_ARG),
+    (dict(eps=-1.0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(dtype=3), gdn.GDN_ERR_INVALID_ARG),
+    (dict(x=None), gdn.GDN_ERR_INVALID_ARG),
+    (dict(y=ctypes.c_void_p(BASE + 64)), gdn.GDN_ERR_INVALID_ARG),  # partial overlap with x
+])
+def test_rownorm_refusals(lib, entry, kw, status):
+    a = dict(x=addr(0), z=addr(1), weight=addr(2), y=addr(3), rows=100, dim=128, eps=1e-6,
+             dtype=1)
+    a.update(kw)
+    if entry == "l2":
+        got = lib.gdn_l2norm_fwd(a["x"], a["y"], a["rows"], a["dim"], a["eps"], a["dtype"], None)
+    else:
+        got = lib.gdn_rmsnorm_gated_fwd(a["x"], a["z"], a["weight"], a["y"], a["rows"], a["dim"],
+                                        a["eps"], a["dtype"], None)
+    assert got == status
+
+
+def test_rmsnorm_needs_its_weight(lib):
+    assert lib.gdn_rmsnorm_gated_fwd(addr(0), None, None, addr(3), 10, 128, 1e-6, 1,
+                                     None) == gdn.GDN_ERR_INVALID_ARG
