@@ -232,6 +232,9 @@ def main():
     if c0.T == 1 and "decode" in c0.name:
         bench_decode(args, rank, world, local_rank, c0, wl, config)
         return
+    if c0.name.startswith("prepost"):
+        bench_prepost(args, rank, world, local_rank, c0, wl, config)
+        return
 
     import torch
     import torch.distributed as dist
@@ -591,6 +594,151 @@ def bench_decode(args, rank, world, local_rank, c0, wl, config):
                            state="updated in place (hT = h0), resident on the device"),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": K, "device_flags": dev_flags}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bench_prepost(args, rank, world, local_rank, c0, wl, config):
+    """One pass of the operations either side of the recurrence over the
+    workload's tokens: causal convolution (width 4, SiLU, with history) of the
+    q, k and v channels, L2 norm of q and k, gated RMS norm of o.  Each is
+    memory-bound; the roofline is HBM for every kernel."""
+    import torch
+    import torch.distributed as dist
+
+    from chunkwise_gated_delta_gdn_gb300 import build as cuda_build
+    from chunkwise_gated_delta_gdn_gb300 import gdn, synth
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    gdn.load(cuda_build.build())
+    xin = synth.make_prepost_inputs(c0)
+    d = {k: v.to(dev) for k, v in xin.items()}
+    B, T, D = d["x"].shape
+    W = d["w"].shape[1]
+    y = torch.empty_like(d["x"])
+    hT = torch.empty_like(d["h0"])
+    qdim = c0.H * c0.dk
+    on = torch.empty_like(d["o"])
+    es = 2
+    n_tok = B * T
+    kbytes = {"conv": 2 * n_tok * D * es, "l2norm_qk": 2 * 2 * n_tok * qdim * es,
+              "rmsnorm_gated": 3 * n_tok * c0.HV * c0.dv * es}
+
+    def conv():
+        gdn.gdn_causal_conv1d_fwd(d["x"], d["w"], d["bias"], d["h0"], y=y, hT=hT,
+                                  activation=gdn.GDN_ACT_SILU)
+
+    # q and k rows (as the recurrence takes them: contiguous [B, T, H, dk] each),
+    # normalised in place
+    qk = torch.empty((2, B, T, c0.H, c0.dk), dtype=c0.dtype, device=dev)
+    qk.copy_(d["x"][..., :2 * qdim].reshape(B, T, 2, c0.H, c0.dk).permute(2, 0, 1, 3, 4))
+
+    def l2_packed():
+        gdn.gdn_l2norm_fwd(qk, eps=1e-6, y=qk)
+
+    def norm():
+        gdn.gdn_rmsnorm_gated_fwd(d["o"], d["norm_weight"], d["z"], eps=1e-6, y=on)
+
+    kern = {"conv": conv, "l2norm_qk": l2_packed, "rmsnorm_gated": norm}
+    for _ in range(args.warmup):
+        for f in kern.values():
+            f()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = {n: [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)] for n in kern}
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.25)
+    main = torch.cuda.current_stream(dev)
+    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_ev.record(main)
+    for i in range(K):
+        for n, f in kern.items():
+            ev[n][2 * i].record(main)
+            f()
+            ev[n][2 * i + 1].record(main)
+    b_ev.record(main)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms_step = a_ev.elapsed_time(b_ev) / K
+    kms = {n: sum(ev[n][2 * i].elapsed_time(ev[n][2 * i + 1]) for i in range(K)) / K for n in kern}
+    peaks, peak_src = load_peaks()
+    per_kernel = {n: {"ms": kms[n], "algorithmic_bytes": kbytes[n],
+                      "achieved_gbs": kbytes[n] / (kms[n] / 1e3) / 1e9,
+                      "frac": kbytes[n] / (kms[n] / 1e3) / 1e9 / peaks["hbm_gbs"]} for n in kern}
+    dom = max(kms, key=kms.get)
+    roofline = {"bound": "hbm", "kernel": {"conv": "gdn_conv1d_kernel",
+                                           "l2norm_qk": "gdn_rownorm_kernel (L2)",
+                                           "rmsnorm_gated": "gdn_rownorm_kernel (gated RMS)"}[dom],
+                "achieved": per_kernel[dom]["achieved_gbs"], "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": per_kernel[dom]["frac"], "traffic": None,
+                "algorithmic_bytes": kbytes[dom], "kernel_ms": kms[dom],
+                "peak_source": f"hbm_gbs of {peak_src}"}
+    value = world * n_tok / (ms_step / 1e3)
+
+    e2e = None
+    if not args.no_e2e:
+        hx = xin["x"].pin_memory()
+        ho, hz = xin["o"].pin_memory(), xin["z"].pin_memory()
+        hy, hon = torch.empty(y.shape, dtype=y.dtype).pin_memory(), torch.empty(on.shape, dtype=on.dtype).pin_memory()
+
+        def e2e_step():
+            d["x"].copy_(hx, non_blocking=True)
+            d["o"].copy_(ho, non_blocking=True)
+            d["z"].copy_(hz, non_blocking=True)
+            conv()
+            l2_packed()
+            norm()
+            hy.copy_(y, non_blocking=True)
+            hon.copy_(on, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e = max(2, min(args.e2e_steps, 5))
+        a2.record(main)
+        for _ in range(n_e):
+            e2e_step()
+        b2.record(main)
+        torch.cuda.synchronize()
+        e_ms = a2.elapsed_time(b2) / n_e
+        h2d = sum(t.numel() * t.element_size() for t in (hx, ho, hz))
+        d2h = sum(t.numel() * t.element_size() for t in (hy, hon))
+        e2e = {"value": world * n_tok / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms, "steps": n_e,
+               "note": "x, o and z copied in, the convolution output and the normed o copied "
+                       "out, one stream"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle  # noqa: F401  (the package; the pre/post oracle is numpy)
+        from oracle import prepost
+        n_s = 512
+        t0 = time.perf_counter()
+        prepost.causal_conv1d(xin["x"][0, :n_s], xin["w"], xin["bias"], xin["h0"][:1], [0, n_s], 1)
+        prepost.l2norm(xin["x"][0, :n_s, :2 * qdim].reshape(n_s, 2 * c0.H, c0.dk), 1e-6)
+        prepost.rmsnorm_gated(xin["o"][0, :n_s], xin["norm_weight"], xin["z"][0, :n_s], 1e-6)
+        sec = time.perf_counter() - t0
+        cpu = {"value": n_s / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"fp64 numpy oracle of the three operations on the first {n_s} tokens "
+                         f"of {c0.name}, {sec:.2f} s"}
+
+    line = {"metric": "pre/post ops tokens/s (causal conv + q/k L2 norm + gated RMS norm, "
+                      "1 GB300) and % of HBM roofline",
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; no dataset)",
+            "config": dict(config, conv_channels=D, conv_width=W, activation="silu",
+                           l2="inputs exceed the 129 MB L2; no flush",
+                           parallelism=f"replicas x{world}"),
+            "roofline": roofline, "kernels": per_kernel, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": K * 4}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -14,11 +14,14 @@
 //    recurrence, stratat pull #1296, re-base notes):
 //        y = x / sqrt(mean(x^2) + eps) * weight [* silu(z)].
 //
-// Convolution layout: one thread owns 8 adjacent channels (one 16-byte bf16
+// Convolution layout: one thread owns 4 adjacent channels (one 8-byte bf16
 // load per token) and walks 32 consecutive tokens, keeping the last W - 1
-// inputs in registers; a warp covers 256 channels of a token with coalesced
-// 512-byte accesses.  A tile re-reads only its W - 1 tokens of halo.  The
-// norms give one warp to a row, each lane a contiguous piece of it.
+// inputs in registers; a warp covers 128 channels of a token with coalesced
+// 256-byte accesses, and loads eight tokens ahead of use.  Four channels keep
+// the thread under 80 registers, so that enough warps share an SM to cover
+// the memory latency.  A tile re-reads
+// only its W - 1 tokens of halo.  The norms give one warp four rows, each lane
+// a contiguous piece of each, all loaded before the first is reduced.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -29,46 +32,60 @@ namespace gdn {
 namespace {
 
 constexpr int kConvThreads = 128;
-constexpr int kConvVec = 8;      // channels per thread
+constexpr int kConvVec = 4;      // channels per thread
 constexpr int kConvTokens = 32;  // tokens per thread
+constexpr int kConvAhead = 8;    // tokens loaded ahead of use
 
+// 4 consecutive elements, raw: one 8-byte load for bf16, one 16-byte for fp32
 template <bool BF16>
-__device__ __forceinline__ void load8(const void *base, size_t elem, float (&v)[8]) {
+struct Raw4;
+template <>
+struct Raw4<true> {
+  uint2 u;
+};
+template <>
+struct Raw4<false> {
+  uint4 u;
+};
+template <bool BF16>
+__device__ __forceinline__ Raw4<BF16> load_raw4(const void *base, size_t elem) {
+  Raw4<BF16> r;
+  if constexpr (BF16)
+    r.u = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(base) + elem));
+  else
+    r.u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const float *>(base) + elem));
+  return r;
+}
+template <bool BF16>
+__device__ __forceinline__ void unpack4(const Raw4<BF16> &r, float (&v)[4]) {
   if constexpr (BF16) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-        static_cast<const __nv_bfloat16 *>(base) + elem));
-    const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const float2 f = __bfloat1622float2(b[i]);
-      v[2 * i] = f.x;
-      v[2 * i + 1] = f.y;
-    }
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.u.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.u.y));
+    v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
   } else {
-    const float *p = static_cast<const float *>(base) + elem;
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(p + 4));
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    v[0] = __uint_as_float(r.u.x); v[1] = __uint_as_float(r.u.y);
+    v[2] = __uint_as_float(r.u.z); v[3] = __uint_as_float(r.u.w);
+  }
+}
+template <bool BF16>
+__device__ __forceinline__ void load4(const void *base, size_t elem, float (&v)[4]) {
+  unpack4<BF16>(load_raw4<BF16>(base, elem), v);
+}
+template <bool BF16>
+__device__ __forceinline__ void store4(void *base, size_t elem, const float (&v)[4]) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(v[0], v[1]);
+    const __nv_bfloat162 b1 = __floats2bfloat162_rn(v[2], v[3]);
+    *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(base) + elem) =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&b0), *reinterpret_cast<const uint32_t *>(&b1));
+  } else {
+    *reinterpret_cast<float4 *>(static_cast<float *>(base) + elem) = make_float4(v[0], v[1], v[2], v[3]);
   }
 }
 
-template <bool BF16>
-__device__ __forceinline__ void store8(void *base, size_t elem, const float (&v)[8]) {
-  if constexpr (BF16) {
-    uint4 raw;
-    __nv_bfloat162 *b = reinterpret_cast<__nv_bfloat162 *>(&raw);
-#pragma unroll
-    for (int i = 0; i < 4; i++) b[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(base) + elem) = raw;
-  } else {
-    float *p = static_cast<float *>(base) + elem;
-    *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
-    *reinterpret_cast<float4 *>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
-  }
-}
-
-__device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
+// SiLU with the fast exponential and division intrinsics: relative error a few
+// units of 2^-22 for |x| < 10, far inside one rounding to bf16 (2^-9)
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
 // sequence holding token `tok` (largest n with start_n <= tok), or -1
 __device__ __forceinline__ int seq_of(const SeqInfo &s, int tok) {
@@ -128,7 +145,7 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv1d_kernel(ConvArgs a) {
     const int tau = tt0 - H + i;
     if (tau >= start) {
       float xv[kConvVec];
-      load8<BF16>(a.x, (size_t)tau * a.D + c0, xv);
+      load4<BF16>(a.x, (size_t)tau * a.D + c0, xv);
 #pragma unroll
       for (int v = 0; v < kConvVec; v++) win[i][v] = xv[v];
     } else {
@@ -136,36 +153,47 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv1d_kernel(ConvArgs a) {
       for (int v = 0; v < kConvVec; v++) win[i][v] = hist(n, tt0 - start + i, v);
     }
   }
-  for (int t = tt0; t < tt1; t++) {
-    if (t >= end) {  // the next non-empty sequence starts at t
-      while (t >= end && n + 1 < a.seq.n_seqs) {
-        n++;
-        start = end;
-        end = seq_start(a.seq, n + 1);
+#pragma unroll 1
+  for (int tb = tt0; tb < tt1; tb += kConvAhead) {
+    // the next kConvAhead tokens' inputs in flight together
+    Raw4<BF16> raw[kConvAhead];
+#pragma unroll
+    for (int u = 0; u < kConvAhead; u++)
+      if (tb + u < tt1) raw[u] = load_raw4<BF16>(a.x, (size_t)(tb + u) * a.D + c0);
+#pragma unroll
+    for (int u = 0; u < kConvAhead; u++) {
+      const int t = tb + u;
+      if (t >= tt1) break;
+      if (t >= end) {  // the next non-empty sequence starts at t
+        while (t >= end && n + 1 < a.seq.n_seqs) {
+          n++;
+          start = end;
+          end = seq_start(a.seq, n + 1);
+        }
+#pragma unroll
+        for (int i = 0; i < H; i++)
+#pragma unroll
+          for (int v = 0; v < kConvVec; v++) win[i][v] = hist(n, i, v);
       }
+      float xv[kConvVec], out[kConvVec];
+      unpack4<BF16>(raw[u], xv);
 #pragma unroll
-      for (int i = 0; i < H; i++)
+      for (int v = 0; v < kConvVec; v++) {
+        float acc = bs[v];
 #pragma unroll
-        for (int v = 0; v < kConvVec; v++) win[i][v] = hist(n, i, v);
-    }
-    float xv[kConvVec], out[kConvVec];
-    load8<BF16>(a.x, (size_t)t * a.D + c0, xv);
+        for (int i = 0; i < H; i++) acc = fmaf(wt[i][v], win[i][v], acc);
+        acc = fmaf(wt[W - 1][v], xv[v], acc);
+        out[v] = SILU ? silu(acc) : acc;
+      }
+      store4<BF16>(a.y, (size_t)t * a.D + c0, out);
 #pragma unroll
-    for (int v = 0; v < kConvVec; v++) {
-      float acc = bs[v];
+      for (int i = 0; i + 1 < H; i++)
 #pragma unroll
-      for (int i = 0; i < H; i++) acc = fmaf(wt[i][v], win[i][v], acc);
-      acc = fmaf(wt[W - 1][v], xv[v], acc);
-      out[v] = SILU ? silu(acc) : acc;
-    }
-    store8<BF16>(a.y, (size_t)t * a.D + c0, out);
+        for (int v = 0; v < kConvVec; v++) win[i][v] = win[i + 1][v];
+      if constexpr (H > 0) {
 #pragma unroll
-    for (int i = 0; i + 1 < H; i++)
-#pragma unroll
-      for (int v = 0; v < kConvVec; v++) win[i][v] = win[i + 1][v];
-    if constexpr (H > 0) {
-#pragma unroll
-      for (int v = 0; v < kConvVec; v++) win[H - 1][v] = xv[v];
+        for (int v = 0; v < kConvVec; v++) win[H - 1][v] = xv[v];
+      }
     }
   }
 }
@@ -200,38 +228,76 @@ __global__ void __launch_bounds__(256) gdn_conv1d_state_kernel(ConvArgs a) {
 // ---------------------------------------------------------------------------
 // row norms: one warp per row, lane l owns elements [l E, l E + E), E = DIM/32
 // ---------------------------------------------------------------------------
+// a lane's E contiguous elements as 32-bit words, in the widest aligned
+// vector loads (E 16-bit or 32-bit elements = E/2 or E words)
+template <int NW>
+__device__ __forceinline__ void ld_words(const uint32_t *p, uint32_t (&w)[NW]) {
+  if constexpr (NW % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 4) {
+      const uint4 u = *reinterpret_cast<const uint4 *>(p + i);
+      w[i] = u.x; w[i + 1] = u.y; w[i + 2] = u.z; w[i + 3] = u.w;
+    }
+  } else if constexpr (NW % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 2) {
+      const uint2 u = *reinterpret_cast<const uint2 *>(p + i);
+      w[i] = u.x; w[i + 1] = u.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW; i++) w[i] = p[i];
+  }
+}
+template <int NW>
+__device__ __forceinline__ void st_words(uint32_t *p, const uint32_t (&w)[NW]) {
+  if constexpr (NW % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 4)
+      *reinterpret_cast<uint4 *>(p + i) = make_uint4(w[i], w[i + 1], w[i + 2], w[i + 3]);
+  } else if constexpr (NW % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 2) *reinterpret_cast<uint2 *>(p + i) = make_uint2(w[i], w[i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW; i++) p[i] = w[i];
+  }
+}
+
 template <int E, bool BF16>
 __device__ __forceinline__ void load_row(const void *base, size_t off, float (&v)[E]) {
   if constexpr (BF16) {
-    const __nv_bfloat16 *p = static_cast<const __nv_bfloat16 *>(base) + off;
+    uint32_t w[E / 2];
+    ld_words<E / 2>(reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(base) + off), w);
 #pragma unroll
-    for (int i = 0; i < E; i += 2) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p + i));
-      v[i] = f.x;
-      v[i + 1] = f.y;
+    for (int i = 0; i < E / 2; i++) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
     }
   } else {
-    const float *p = static_cast<const float *>(base) + off;
+    uint32_t w[E];
+    ld_words<E>(reinterpret_cast<const uint32_t *>(static_cast<const float *>(base) + off), w);
 #pragma unroll
-    for (int i = 0; i < E; i += 2) {
-      const float2 f = *reinterpret_cast<const float2 *>(p + i);
-      v[i] = f.x;
-      v[i + 1] = f.y;
-    }
+    for (int i = 0; i < E; i++) v[i] = __uint_as_float(w[i]);
   }
 }
 
 template <int E, bool BF16>
 __device__ __forceinline__ void store_row(void *base, size_t off, const float (&v)[E]) {
   if constexpr (BF16) {
-    __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(base) + off;
+    uint32_t w[E / 2];
 #pragma unroll
-    for (int i = 0; i < E; i += 2)
-      *reinterpret_cast<__nv_bfloat162 *>(p + i) = __floats2bfloat162_rn(v[i], v[i + 1]);
+    for (int i = 0; i < E / 2; i++) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    st_words<E / 2>(reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(base) + off), w);
   } else {
-    float *p = static_cast<float *>(base) + off;
+    uint32_t w[E];
 #pragma unroll
-    for (int i = 0; i < E; i += 2) *reinterpret_cast<float2 *>(p + i) = make_float2(v[i], v[i + 1]);
+    for (int i = 0; i < E; i++) w[i] = __float_as_uint(v[i]);
+    st_words<E>(reinterpret_cast<uint32_t *>(static_cast<float *>(base) + off), w);
   }
 }
 
@@ -241,45 +307,43 @@ __device__ __forceinline__ float warp_sum(float s) {
   return s;
 }
 
-template <int DIM, bool BF16>
-__global__ void __launch_bounds__(256) gdn_l2norm_kernel(RowNormArgs a) {
+// RPW rows per warp, all loaded before the first is reduced, so that each
+// lane keeps several loads in flight.  KIND 0: L2 norm; 1: gated RMS norm.
+template <int DIM, bool BF16, int KIND, int RPW>
+__global__ void __launch_bounds__(256) gdn_rownorm_kernel(RowNormArgs a) {
   constexpr int E = DIM / 32;
-  const long row = blockIdx.x * 8L + (threadIdx.x >> 5);
-  if (row >= a.rows) return;
+  const long row0 = (blockIdx.x * 8L + (threadIdx.x >> 5)) * RPW;
   const int lane = threadIdx.x & 31;
-  const size_t off = (size_t)row * DIM + lane * E;
-  float v[E];
-  load_row<E, BF16>(a.x, off, v);
-  float s = 0.f;
+  float v[RPW][E], z[RPW][E];
 #pragma unroll
-  for (int i = 0; i < E; i++) s = fmaf(v[i], v[i], s);
-  const float r = rsqrtf(warp_sum(s) + a.eps);
-#pragma unroll
-  for (int i = 0; i < E; i++) v[i] *= r;
-  store_row<E, BF16>(a.y, off, v);
-}
-
-template <int DIM, bool BF16>
-__global__ void __launch_bounds__(256) gdn_rmsnorm_gated_kernel(RowNormArgs a) {
-  constexpr int E = DIM / 32;
-  const long row = blockIdx.x * 8L + (threadIdx.x >> 5);
-  if (row >= a.rows) return;
-  const int lane = threadIdx.x & 31;
-  const size_t off = (size_t)row * DIM + lane * E;
-  float v[E];
-  load_row<E, BF16>(a.x, off, v);
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < E; i++) s = fmaf(v[i], v[i], s);
-  const float r = rsqrtf(warp_sum(s) * (1.f / DIM) + a.eps);
-  float z[E];
-  if (a.z) load_row<E, BF16>(a.z, off, z);
-#pragma unroll
-  for (int i = 0; i < E; i++) {
-    v[i] = v[i] * r * __ldg(a.weight + lane * E + i);
-    if (a.z) v[i] *= silu(z[i]);
+  for (int q = 0; q < RPW; q++) {
+    if (row0 + q < a.rows) {
+      const size_t off = (size_t)(row0 + q) * DIM + lane * E;
+      load_row<E, BF16>(a.x, off, v[q]);
+      if (KIND == 1 && a.z) load_row<E, BF16>(a.z, off, z[q]);
+    }
   }
-  store_row<E, BF16>(a.y, off, v);
+#pragma unroll
+  for (int q = 0; q < RPW; q++) {
+    if (row0 + q >= a.rows) break;
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < E; i++) s = fmaf(v[q][i], v[q][i], s);
+    s = warp_sum(s);
+    if constexpr (KIND == 0) {
+      const float r = rsqrtf(s + a.eps);
+#pragma unroll
+      for (int i = 0; i < E; i++) v[q][i] *= r;
+    } else {
+      const float r = rsqrtf(s * (1.f / DIM) + a.eps);
+#pragma unroll
+      for (int i = 0; i < E; i++) {
+        v[q][i] = v[q][i] * r * __ldg(a.weight + lane * E + i);
+        if (a.z) v[q][i] *= silu(z[q][i]);
+      }
+    }
+    store_row<E, BF16>(a.y, (size_t)(row0 + q) * DIM + lane * E, v[q]);
+  }
 }
 
 template <int W, bool BF16>
@@ -303,11 +367,11 @@ cudaError_t conv_w(const ConvArgs &a, int act, cudaStream_t s) {
 
 template <int DIM, bool BF16>
 cudaError_t rows_dim(const RowNormArgs &a, int kind, cudaStream_t s) {
-  const unsigned grid = (unsigned)((a.rows + 7) / 8);
+  // L2: four rows per warp; gated RMS (two input streams): two
   if (kind == 0)
-    gdn_l2norm_kernel<DIM, BF16><<<grid, 256, 0, s>>>(a);
+    gdn_rownorm_kernel<DIM, BF16, 0, 4><<<(unsigned)((a.rows + 31) / 32), 256, 0, s>>>(a);
   else
-    gdn_rmsnorm_gated_kernel<DIM, BF16><<<grid, 256, 0, s>>>(a);
+    gdn_rownorm_kernel<DIM, BF16, 1, 2><<<(unsigned)((a.rows + 15) / 16), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

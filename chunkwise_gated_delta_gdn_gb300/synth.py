@@ -101,6 +101,13 @@ WORKLOADS = {
                                  dk=128, dv=128, chunk=64, dtype=torch.bfloat16,
                                  gate_mode=GATE_SCALAR, gate_dist="uniform",
                                  gate_low=-5.0, h0_std=0.1),
+    # the operations either side of the recurrence at the 32k spot: causal
+    # convolution (width 4, SiLU) over the q, k and v channels together
+    # ((2 H dk + HV dv) = 10240), L2 norm of q and k, gated RMS norm of o
+    "prepost_bf16_t32768": Case("prepost_bf16_t32768", B=1, T=32768, H=16, HV=48, dk=128,
+                                dv=128, chunk=64, dtype=torch.bfloat16,
+                                gate_mode=GATE_SCALAR, gate_dist="uniform", gate_low=-5.0,
+                                h0_std=None),
     "kda_decode_bf16_b256": Case("kda_decode_bf16_b256", B=256, T=1, H=32, HV=32,
                                  dk=128, dv=128, chunk=32, dtype=torch.bfloat16,
                                  gate_mode=GATE_PER_KEY, gate_dist="uniform",
@@ -180,6 +187,25 @@ def make_inputs(c: Case, lengths: Optional[Sequence[int]] = None) -> dict:
         out["cu_seqlens"] = None
         out["lengths"] = [T] * c.B
     return out
+
+
+def make_prepost_inputs(c: Case, width: int = 4) -> dict:
+    """Seeded inputs of the pre/post operations for the geometry of ``c``:
+    the convolution's input x [B, T, 2 H dk + HV dv] (q, k and v channels
+    side by side) with weights [D, width], bias [D] and history
+    [B, D, width - 1]; the output rows o and gate rows z [B, T, HV, dv] with
+    the norm weight [dv]."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(c.seed + 1000)
+    D = 2 * c.H * c.dk + c.HV * c.dv
+    x = torch.randn((c.B, c.T, D), generator=gen, dtype=torch.float32).to(c.dtype)
+    w = (torch.rand((D, width), generator=gen) * 2 - 1) / width ** 0.5
+    bias = torch.randn(D, generator=gen) * 0.1
+    h0 = torch.randn((c.B, D, width - 1), generator=gen)
+    o = torch.randn((c.B, c.T, c.HV, c.dv), generator=gen, dtype=torch.float32).to(c.dtype)
+    z = torch.randn((c.B, c.T, c.HV, c.dv), generator=gen, dtype=torch.float32).to(c.dtype)
+    wn = torch.rand(c.dv, generator=gen) + 0.5
+    return dict(x=x, w=w, bias=bias, h0=h0, o=o, z=z, norm_weight=wn)
 
 
 def sweep_cases() -> list[Case]:
