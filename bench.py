@@ -677,7 +677,8 @@ def bench_prepost(args, rank, world, local_rank, c0, wl, config):
                                            "l2norm_qk": "gdn_rownorm_kernel (L2)",
                                            "rmsnorm_gated": "gdn_rownorm_kernel (gated RMS)"}[dom],
                 "achieved": per_kernel[dom]["achieved_gbs"], "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": per_kernel[dom]["frac"], "traffic": None,
+                "unit": "GB/s", "frac": per_kernel[dom]["frac"],
+                "traffic": measured_traffic(c0.name, dom, n_tok)[0],
                 "algorithmic_bytes": kbytes[dom], "kernel_ms": kms[dom],
                 "peak_source": f"hbm_gbs of {peak_src}"}
     value = world * n_tok / (ms_step / 1e3)
