@@ -116,6 +116,31 @@ def measured_traffic(workload, kernel, units):
 
 
 # ---------------------------------------------------------------------------
+# ranks: one process per GPU, independent replicas, timed by the slowest
+# ---------------------------------------------------------------------------
+def rank_barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def max_over_ranks(x: float, dev) -> float:
+    """The largest x over all ranks (every rank gets the slowest rank's time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, ms_step: float, world: int) -> float:
+    """Units all ranks processed per second at the slowest rank's step time."""
+    return world * units_per_rank / (ms_step / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
@@ -328,13 +353,9 @@ def main():
         dist.barrier()
     clocks = sampler.stop()
     ms_total = ev_start.elapsed_time(ev_end)
-    ms_step = ms_total / K
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_total / K, dev)
     tokens_per_rank = c0.tokens
-    value = world * tokens_per_rank / (ms_step / 1e3)
+    value = whole_job_rate(tokens_per_rank, ms_step, world)
 
     # ---- end to end through the public binding, host buffers ----
     # Every step copies its inputs in from pinned host memory and its results
@@ -394,12 +415,8 @@ def main():
             e2e_step(i)
         b_ev.record(s_out)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b_ev) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * tokens_per_rank / (e2e_ms / 1e3), "unit": UNIT,
+        e2e_ms = max_over_ranks(a.elapsed_time(b_ev) / args.e2e_steps, dev)
+        e2e = {"value": whole_job_rate(tokens_per_rank, e2e_ms, world), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                "pipeline": "double-buffered; copies in, forward pass and copies out on "
@@ -523,12 +540,8 @@ def bench_decode(args, rank, world, local_rank, c0, wl, config):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms_step = a.elapsed_time(b) / K
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * c0.B / (ms_step / 1e3)
+    ms_step = max_over_ranks(a.elapsed_time(b) / K, dev)
+    value = whole_job_rate(c0.B, ms_step, world)
 
     # end to end: each step's token inputs copied in from pinned host memory
     # and its outputs o copied back; the states stay resident on the device
@@ -553,8 +566,8 @@ def bench_decode(args, rank, world, local_rank, c0, wl, config):
             o_host.copy_(o, non_blocking=True)
         b2.record(main)
         torch.cuda.synchronize()
-        e2e_ms = a2.elapsed_time(b2) / args.e2e_steps
-        e2e = {"value": world * c0.B / (e2e_ms / 1e3), "unit": UNIT,
+        e2e_ms = max_over_ranks(a2.elapsed_time(b2) / args.e2e_steps, dev)
+        e2e = {"value": whole_job_rate(c0.B, e2e_ms, world), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                "note": "token inputs in and o out every step on one stream; the states "
@@ -650,6 +663,7 @@ def bench_prepost(args, rank, world, local_rank, c0, wl, config):
         for f in kern.values():
             f()
     torch.cuda.synchronize()
+    rank_barrier()
     K = args.steps
     ev = {n: [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)] for n in kern}
     sampler = ClockSampler(dev.index)
@@ -665,8 +679,9 @@ def bench_prepost(args, rank, world, local_rank, c0, wl, config):
             ev[n][2 * i + 1].record(main)
     b_ev.record(main)
     torch.cuda.synchronize()
+    rank_barrier()
     clocks = sampler.stop()
-    ms_step = a_ev.elapsed_time(b_ev) / K
+    ms_step = max_over_ranks(a_ev.elapsed_time(b_ev) / K, dev)
     kms = {n: sum(ev[n][2 * i].elapsed_time(ev[n][2 * i + 1]) for i in range(K)) / K for n in kern}
     peaks, peak_src = load_peaks()
     per_kernel = {n: {"ms": kms[n], "algorithmic_bytes": kbytes[n],
@@ -681,7 +696,7 @@ def bench_prepost(args, rank, world, local_rank, c0, wl, config):
                 "traffic": measured_traffic(c0.name, dom, n_tok)[0],
                 "algorithmic_bytes": kbytes[dom], "kernel_ms": kms[dom],
                 "peak_source": f"hbm_gbs of {peak_src}"}
-    value = world * n_tok / (ms_step / 1e3)
+    value = whole_job_rate(n_tok, ms_step, world)
 
     e2e = None
     if not args.no_e2e:
@@ -708,10 +723,11 @@ def bench_prepost(args, rank, world, local_rank, c0, wl, config):
             e2e_step()
         b2.record(main)
         torch.cuda.synchronize()
-        e_ms = a2.elapsed_time(b2) / n_e
+        e_ms = max_over_ranks(a2.elapsed_time(b2) / n_e, dev)
         h2d = sum(t.numel() * t.element_size() for t in (hx, ho, hz))
         d2h = sum(t.numel() * t.element_size() for t in (hy, hon))
-        e2e = {"value": world * n_tok / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e2e = {"value": whole_job_rate(n_tok, e_ms, world), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms, "steps": n_e,
                "note": "x, o and z copied in, the convolution output and the normed o copied "
                        "out, one stream"}
