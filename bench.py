@@ -30,6 +30,18 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "prefill tokens/s (gated delta-rule fwd, 1 GB300) and % of HBM/tensor roofline"
+METRIC_DECODE = "decode tokens/s (gated delta-rule step, T = 1, 1 GB300) and % of HBM roofline"
+METRIC_PREPOST = ("pre/post ops tokens/s (causal conv + q/k L2 norm + gated RMS norm, 1 GB300) "
+                  "and % of HBM roofline")
+
+
+def metric_of(c) -> str:
+    """The metric a workload's line reports (the same for both arms)."""
+    if c.name.startswith("prepost"):
+        return METRIC_PREPOST
+    if c.T == 1 and "decode" in c.name:
+        return METRIC_DECODE
+    return METRIC
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "gdn_bf16_t32768"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -626,8 +638,7 @@ def bench_decode(args, rank, world, local_rank, c0, wl, config):
                "sample": f"fp64 token-serial oracle, {n_done // c0.B} whole decode steps of "
                          f"{c0.name} ({c0.B} sequences x {c0.HV} value heads), {sec:.1f} s"}
 
-    line = {"metric": "decode tokens/s (gated delta-rule step, T = 1, 1 GB300) and % of HBM "
-                      "roofline",
+    line = {"metric": METRIC_DECODE,
             "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": wl.dtype_name, "data": "synthetic (seeded; no dataset)",
@@ -775,8 +786,7 @@ def bench_prepost(args, rank, world, local_rank, c0, wl, config):
                "sample": f"fp64 numpy oracle of the three operations on the first {n_s} tokens "
                          f"of {c0.name}, {sec:.2f} s"}
 
-    line = {"metric": "pre/post ops tokens/s (causal conv + q/k L2 norm + gated RMS norm, "
-                      "1 GB300) and % of HBM roofline",
+    line = {"metric": METRIC_PREPOST,
             "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; no dataset)",
@@ -798,27 +808,50 @@ def run_reference(args, rank, world, c0, wl, config):
     import oracle
     from chunkwise_gated_delta_gdn_gb300 import synth
 
-    x = synth.make_inputs(c0)
     total = args.steps + args.warmup
     per_step_s = min(10.0, 150.0 / max(total, 1))
-    n_tok = calibrate_oracle(wl, x, per_step_s)
+    if c0.name.startswith("prepost"):
+        # the pre/post operations' numpy oracle on a prefix of the tokens
+        from oracle import prepost
+        xin = synth.make_prepost_inputs(c0)
+        qdim = c0.H * c0.dk
+
+        def sample(n_s):
+            t0 = time.perf_counter()
+            prepost.causal_conv1d(xin["x"][0, :n_s], xin["w"], xin["bias"], xin["h0"][:1],
+                                  [0, n_s], prepost.ACT_SILU)
+            prepost.l2norm(xin["x"][0, :n_s, :2 * qdim].reshape(n_s, 2 * c0.H, c0.dk), 1e-6)
+            prepost.rmsnorm_gated(xin["o"][0, :n_s], xin["norm_weight"], xin["z"][0, :n_s], 1e-6)
+            return time.perf_counter() - t0, n_s
+
+        sec, n_s = sample(64)
+        n_tok = int(min(c0.T, max(64, per_step_s / max(sec / n_s, 1e-9))))
+        what = f"the numpy fp64 oracle of the three operations on the first {n_tok} tokens"
+        cores = 1
+    else:
+        x = synth.make_inputs(c0)
+        n_tok = calibrate_oracle(wl, x, per_step_s)
+
+        def sample(n_s):
+            return oracle_sample(wl, x, n_s)
+
+        what = f"fp64 token-serial oracle on the first {n_tok} tokens (all {c0.HV} value heads)"
+        cores = oracle.num_threads()
     for _ in range(args.warmup):
-        oracle_sample(wl, x, n_tok)
+        sample(n_tok)
     times, n = [], 0
     for _ in range(args.steps):
-        sec, n = oracle_sample(wl, x, n_tok)
+        sec, n = sample(n_tok)
         times.append(sec)
     ms_step = 1e3 * sum(times) / len(times)
     value = n / (ms_step / 1e3)
-    cores = oracle.num_threads()
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+    line = {"impl": "reference", "metric": metric_of(c0), "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; no dataset)",
             "config": config,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"each step: fp64 token-serial oracle on the first {n} "
-                                       f"tokens (all {c0.HV} value heads) of {c0.name}"},
+                             "sample": f"each step: {what} of {c0.name}"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
