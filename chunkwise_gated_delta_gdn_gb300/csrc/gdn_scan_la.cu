@@ -10,14 +10,16 @@
 // chunk).  Computing X_c from S_c puts two tensor-core round trips on the
 // serial path.  Expanding S_c instead gives
 //   X_c = d_{c-1} (K_c S_{c-1}) + E_c Y_{c-1},   E_c = K_c P1_{c-1},
-// with E_c state-independent (written by the prep kernel).  K_c S_{c-1} is
-// issued a full chunk ahead, stacked with Q_{c-1} S_{c-1}, so only the
-// K = C product E_c Y_{c-1} sits between Y_{c-1} and Y_c.  Per chunk:
-//   MMA2(c) = P1_{c-1} Y_{c-1}               -> D2       (state update)
-//   MMA1(c) = [E_c; AqkT_{c-1}] Y_{c-1}      -> D1[c&1]  (X_c part, O_{c-1} part)
-//   MMA3(c) = [K_{c+1}; Q_c] S_c             -> D3[c&1]  (after S_c is known)
+// with E_c state-independent (written by the prep kernel).  Per chunk c, in
+// this order on the tensor pipe:
+//   MMA1(c) = [E_c; AqkT_{c-1}] Y_{c-1}      -> D1[c%3]     (X_c part, O_{c-1} part)
+//   MMA3(c) = [K_c; Q_{c-1}] S_{c-1}         -> D3[(c-1)&1] (X_c part, O_{c-1} part)
+//   MMA2(c) = P1_{c-1} Y_{c-1}               -> D2          (state update)
 // all M = 128, N = 64 (a dv slice), fp16 operands, fp32 accumulation in
-// tensor memory; the tensor pipe runs them back to back.
+// tensor memory.  The chain forms Y_c as soon as MMA1(c) and MMA3(c) are
+// done, and only then S_c = d_{c-1} S_{c-1} + D2, whose fp16 image feeds
+// MMA3(c + 1): the state update stays off the path from Y_{c-1} to Y_c,
+// where MMA3(c) overlaps the chain's loads of chunk c's coefficients and V.
 //
 // One CTA per (sequence, value head, 64-column slice of dv), 384 threads:
 //  * warps 0-7 (the chain): warp w owns tensor-memory lanes 32 (w % 4) .. +31
@@ -27,6 +29,8 @@
 //    lanes 64..64+C-1 form O (query rows), lanes below dk update the state.
 //  * warp 8, one thread: issues every tensor-core product, the TMA loads of V
 //    (a three-deep ring) and the bulk copies of the prep images (three deep).
+//    Y is double-buffered (MMA2(c) may still read Y_{c-1} while Y_c is
+//    written) and D1 triple-buffered (the query lanes read it one chunk late).
 //  * warp 9: gates and beta by cp.async, cumulative gates and the per-row
 //    coefficients (a four-deep ring).
 //  * warps 10-11: the [K_{c+1}; Q_c] operand (a two-deep ring): bulk copies of
@@ -65,7 +69,7 @@ struct LaSmem {
   static constexpr int KQ = (DK / 64) * 16384;  // [K_{c+1}; Q_c], K-major, 128 rows
   static constexpr int PI = kLaImageBytes;       // [P1; E; AqkT]
   static constexpr int SI = (DK / 8) * 1024;     // S, MN-major, dk K-rows
-  static constexpr int YI = 8 * 1024;            // Y, MN-major, 64 K-rows
+  static constexpr int YI = 8 * 1024;            // Y, MN-major, 64 K-rows (x2, by chunk parity)
   static constexpr int VI = C * 128;             // V slice, C rows x 64 bf16 (x NV)
   // per chunk: raw gates and beta (2C), then beta, gam, scale*gam (3C), decay
   static constexpr int CF = (5 * C + 4) * 4;
@@ -73,7 +77,7 @@ struct LaSmem {
   static constexpr int kP = kKQ + NKQ * KQ;
   static constexpr int kS = kP + NP * PI;
   static constexpr int kY = kS + SI;
-  static constexpr int kV = kY + YI;
+  static constexpr int kV = kY + 2 * YI;
   static constexpr int kCf = kV + NV * VI;
   static constexpr int kBar = kCf + NCF * CF;
   enum {
@@ -84,8 +88,8 @@ struct LaSmem {
     B_CFFULL = B_PFULL + NP,
     B_CFREADY = B_CFFULL + NCF,
     B_CFEMPTY = B_CFREADY + NCF,
-    B_MMA1 = B_CFEMPTY + NCF,  // two, by chunk parity
-    B_MMA2 = B_MMA1 + 2,
+    B_MMA1 = B_CFEMPTY + NCF,  // three, by chunk index mod 3
+    B_MMA2 = B_MMA1 + 3,
     B_MMA3 = B_MMA2 + 1,       // two, by chunk parity
     B_SREADY = B_MMA3 + 2,
     B_YREADY = B_SREADY + 1,
@@ -150,10 +154,8 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       mbar_init(bar(SM::B_CFREADY + s), 32);
       mbar_init(bar(SM::B_CFEMPTY + s), kChain / 32);
     }
-    for (int i = 0; i < 2; i++) {
-      mbar_init(bar(SM::B_MMA1 + i), 1);
-      mbar_init(bar(SM::B_MMA3 + i), 1);
-    }
+    for (int i = 0; i < 3; i++) mbar_init(bar(SM::B_MMA1 + i), 1);
+    for (int i = 0; i < 2; i++) mbar_init(bar(SM::B_MMA3 + i), 1);
     for (int i = 0; i < SM::NV; i++) mbar_init(bar(SM::B_VFULL + i), 1);
     mbar_init(bar(SM::B_MMA2), 1);
     mbar_init(bar(SM::B_SREADY), kChain / 32);
@@ -161,16 +163,16 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     *abort_flag = 0;
     mbar_fence_init();
   }
-  constexpr uint32_t kTmemCols = 512;  // D1 x2, D2, D3 x2: 5 x NS columns
+  constexpr uint32_t kTmemCols = 512;  // D1 x3, D2, D3 x2: 6 x NS columns
   if (warp == 0) tmem_alloc(smem_addr(tslot), kTmemCols);
-  for (int i = tid; i < SM::YI / 16; i += kThreads)
+  for (int i = tid; i < 2 * SM::YI / 16; i += kThreads)
     reinterpret_cast<uint4 *>(sm + SM::kY)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tslot;
-  const uint32_t tD1 = tmem, tD2 = tmem + 2 * NS, tD3 = tmem + 3 * NS;
+  const uint32_t tD1 = tmem, tD2 = tmem + 3 * NS, tD3 = tmem + 4 * NS;
   constexpr uint32_t idesc = idesc_f16(128, NS, 0, 1);
 
   if (warp < 8) {
@@ -222,8 +224,9 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     bool nonfinite = false;
     // ---- O_cc = scale gam Q_cc S_cc + AqkT_cc Y_cc (query lanes) ----
     // Q_cc S_cc is in D3[cc & 1] (MMA3(cc + 1)), AqkT_cc Y_cc in
-    // D1[(cc + 1) & 1] (MMA1(cc + 1)); both stay until this thread's next
-    // SREADY arrival, which the products overwriting them wait for.  The
+    // D1[(cc + 1) % 3] (MMA1(cc + 1)).  The products that overwrite them,
+    // MMA3(cc + 3) and MMA1(cc + 4), are issued only after SREADY(cc + 2),
+    // which this thread joins after writing the output.  The
     // output of chunk cc is written at the top of iteration cc + 2, while
     // the tensor pipe runs the state products, so that its tensor-memory
     // reads and global stores stay out of the window in which the key lanes
@@ -234,7 +237,7 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       const int L = min(C, end - t0);
       float qs[NH], d[NH];
       lane_half(tD3 + (cc & 1) * NS, qs);
-      lane_half(tD1 + ((cc + 1) & 1) * NS, d);
+      lane_half(tD1 + ((cc + 1) % 3) * NS, d);
       if (r < L) {
         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((long)(t0 + r) * a.HV + hv) * a.dv + col0 + c0;
 #pragma unroll
@@ -283,24 +286,12 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
             vv[ch] = *reinterpret_cast<const uint4 *>(vrow + (((c0 / 8 + ch) ^ (t & 7)) << 4));
         }
         if (query_warp && c >= 2) output(c - 2, sgam_prev2);
-        // ---- state: S_c = d_{c-1} S_{c-1} + P1_{c-1} Y_{c-1} ----
-        if (c >= 1) {
-          mbar_wait(bar(SM::B_MMA2), (c - 1) & 1, abort_flag);
-          fence_after_sync();
-          if (state_warp) {
-            float d[NH];
-            lane_half(tD2, d);
-#pragma unroll
-            for (int i = 0; i < NH; i++) s_reg[i] = fmaf(dec_prev, s_reg[i], d[i]);
-            if (c < nch) write_state_image();
-          }
-          if (c < nch) signal(SM::B_SREADY);
-          mbar_wait(bar(SM::B_MMA1 + (c & 1)), ((c - 1) >> 1) & 1, abort_flag);
-        }
-        // K_c S_{c-1} and Q_{c-1} S_{c-1} (chunk 0: K_0 S_0)
+        // X_c's products: E_c Y_{c-1} (MMA1(c)) and K_c S_{c-1} (MMA3(c); chunk
+        // 0: K_0 S_0)
+        if (c >= 1) mbar_wait(bar(SM::B_MMA1 + c % 3), ((c - 1) / 3) & 1, abort_flag);
         mbar_wait(bar(SM::B_MMA3 + ((c - 1) & 1)), (c >> 1) & 1, abort_flag);
         fence_after_sync();
-        const uint32_t d3 = tD3 + ((c - 1) & 1) * NS, d1 = tD1 + (c & 1) * NS;
+        const uint32_t d3 = tD3 + ((c - 1) & 1) * NS, d1 = tD1 + (c % 3) * NS;
 
         if (key_warp && c < nch) {
           // ---- Y_c = beta (V - gam X), X = d_{c-1} K_c S_{c-1} + E_c Y_{c-1} ----
@@ -312,6 +303,7 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
 #pragma unroll
             for (int i = 0; i < NH; i++) x[i] = fmaf(dec_prev, x[i], e[i]);
           }
+          unsigned char *ybuf = sm + SM::kY + (c & 1) * SM::YI;
 #pragma unroll
           for (int ch = 0; ch < NH / 8; ch++) {
             const __nv_bfloat162 *vb = reinterpret_cast<const __nv_bfloat162 *>(&vv[ch]);
@@ -323,9 +315,23 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
               ph[i] = __floats2half2_rn(beta_r * (vf.x - gam_r * x[ch * 8 + 2 * i]),
                                         beta_r * (vf.y - gam_r * x[ch * 8 + 2 * i + 1]));
             }
-            *reinterpret_cast<uint4 *>(sm + SM::kY + mnmajor_chunk_off(t, c0 / 8 + ch, 64)) = pk;
+            *reinterpret_cast<uint4 *>(ybuf + mnmajor_chunk_off(t, c0 / 8 + ch, 64)) = pk;
           }
           signal(SM::B_YREADY);
+        }
+        // ---- state, after Y_c: S_c = d_{c-1} S_{c-1} + P1_{c-1} Y_{c-1} ----
+        // (its product MMA3(c + 1) is needed only by X_{c+1})
+        if (c >= 1) {
+          mbar_wait(bar(SM::B_MMA2), (c - 1) & 1, abort_flag);
+          fence_after_sync();
+          if (state_warp) {
+            float d[NH];
+            lane_half(tD2, d);
+#pragma unroll
+            for (int i = 0; i < NH; i++) s_reg[i] = fmaf(dec_prev, s_reg[i], d[i]);
+            if (c < nch) write_state_image();
+          }
+          if (c < nch) signal(SM::B_SREADY);
         }
         dec_prev = dec_c;
         sgam_prev2 = sgam_prev;
@@ -384,34 +390,39 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
       if (nch > 1) issue_p(1);
       mbar_wait(bar(SM::B_SREADY), 0, abort_flag);  // S_0 image
       mma3(0, 1);  // [K_0; Q_0] S_0 -> D3[1] (read as "chunk -1")
-      mma3(1, 0);  // [K_1; Q_0] S_0 -> D3[0]
+      // Per chunk, in this order: MMA1(c) and MMA3(c) give X_c (the serial
+      // path), MMA2(c) the next state (needed only after Y_c).
       for (int c = 1; c <= nch; c++) {
         mbar_wait(bar(SM::B_YREADY), (c - 1) & 1, abort_flag);  // Y_{c-1}, V_{c-1} consumed
         const int ps = (c - 1) % NP;
         mbar_wait(bar(SM::B_PFULL + ps), ((c - 1) / NP) & 1, abort_flag);
         fence_after_sync();
         const uint32_t sP = smem_addr(sm + SM::kP + ps * SM::PI);
+        const uint32_t sYp = sY + ((c - 1) & 1) * SM::YI;  // Y_{c-1}
 #pragma unroll
         for (int k0 = 0; k0 < C; k0 += 16) {
-          const uint64_t bd = make_desc(sY + (k0 >> 4) * 2048, 8 * 1024, 1024);
+          const uint64_t bd = make_desc(sYp + (k0 >> 4) * 2048, 8 * 1024, 1024);
+          mma_f16(tD1 + (c % 3) * NS, make_desc(sP + 128 * 128 + k0 * 2, 16, 1024), bd, idesc,
+                  k0 > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(SM::B_MMA1 + c % 3));
+        // S_{c-1} image (chunk 1: S_0, waited above)
+        mbar_wait(bar(SM::B_SREADY), (c - 1) & 1, abort_flag);
+        mma3(c, (c - 1) & 1);  // [K_c; Q_{c-1}] S_{c-1}
+#pragma unroll
+        for (int k0 = 0; k0 < C; k0 += 16) {
+          const uint64_t bd = make_desc(sYp + (k0 >> 4) * 2048, 8 * 1024, 1024);
           mma_f16(tD2, make_desc(sP + k0 * 2, 16, 1024), bd, idesc, k0 > 0 ? 1u : 0u);
         }
         mma_commit(bar(SM::B_MMA2));
-#pragma unroll
-        for (int k0 = 0; k0 < C; k0 += 16) {
-          const uint64_t bd = make_desc(sY + (k0 >> 4) * 2048, 8 * 1024, 1024);
-          mma_f16(tD1 + (c & 1) * NS, make_desc(sP + 128 * 128 + k0 * 2, 16, 1024), bd, idesc,
-                  k0 > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(SM::B_MMA1 + (c & 1)));
-        // loads for later chunks, after the products on the serial path: V of
-        // chunk c + 2 into the buffer V_{c-1} left, the prep image of chunk
-        // c + 1 into the slot that MMA2(c-1) and MMA1(c-1) have finished with
+        // loads for later chunks, off the serial path: V of chunk c + 2 into
+        // the buffer V_{c-1} left; the prep image of chunk c + 1 into the slot
+        // of chunk c - 2, once MMA1(c) is done (the pipe runs in order, so
+        // MMA2(c - 1), that slot's last reader, is done too)
         if (c + 2 < nch) issue_v(c + 2);
-        if (c + 1 < nch) issue_p(c + 1);
-        if (c < nch) {
-          mbar_wait(bar(SM::B_SREADY), c & 1, abort_flag);  // S_c image
-          mma3(c + 1, c & 1);                               // [K_{c+1}; Q_c] S_c
+        if (c + 1 < nch) {
+          mbar_wait(bar(SM::B_MMA1 + c % 3), ((c - 1) / 3) & 1, abort_flag);
+          issue_p(c + 1);
         }
       }
     }
