@@ -21,7 +21,8 @@
 // MMA3(c + 1): the state update stays off the path from Y_{c-1} to Y_c,
 // where MMA3(c) overlaps the chain's loads of chunk c's coefficients and V.
 //
-// One CTA per (sequence, value head, 64-column slice of dv), 384 threads:
+// One CTA per (sequence, value head, 64-column slice of dv), 384 threads,
+// longest packed sequences first:
 //  * warps 0-7 (the chain): warp w owns tensor-memory lanes 32 (w % 4) .. +31
 //    and columns 32 (w / 4) .. +31 of the slice.  The fp32 state slice
 //    (dk x 64) lives in registers for the whole sequence; an fp16 copy in
@@ -59,6 +60,7 @@ constexpr int kCoefWarp = 9;
 constexpr int kKqWarp0 = 10;      // warps 10-11
 constexpr int kKqThreads = 64;
 constexpr int kThreads = 384;
+constexpr int kLptSeqs = 64;      // packed sequences ranked by length per block
 constexpr int NS = kScanTcSlice;
 constexpr int NH = NS / 2;  // columns per chain thread
 static_assert(NS == 64, "one 128-byte swizzle atom per S / Y row");
@@ -127,8 +129,31 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SM::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SM::kMisc + 4);
 
-  const int n = blockIdx.x, hv = blockIdx.y, col0 = blockIdx.z * NS;
+  // Blocks are launched in index order, and every block of a (sequence, value
+  // head, slice) runs that sequence's whole chain.  Block index = rank * HV *
+  // slices + head * slices + slice, and for packed input of up to kLptSeqs
+  // sequences the rank counts sequences by decreasing length (ties by index):
+  // the longest chains start first, so the short ones fill in behind them
+  // instead of a long chain starting last.
+  const int n_slices = a.dv / NS;
+  const int rank = blockIdx.x / (a.HV * n_slices);
+  const int hv = (blockIdx.x / n_slices) % a.HV, col0 = (blockIdx.x % n_slices) * NS;
   const int hq = hv / (a.HV / a.H);
+  int n = rank;
+  if (a.seq.cu && a.seq.n_seqs <= kLptSeqs) {
+    int *pick = reinterpret_cast<int *>(sm + SM::kMisc + 8);
+    for (int i = tid; i < a.seq.n_seqs; i += kThreads) {
+      const int li = __ldg(a.seq.cu + i + 1) - __ldg(a.seq.cu + i);
+      int longer = 0;
+      for (int j = 0; j < a.seq.n_seqs; j++) {
+        const int lj = __ldg(a.seq.cu + j + 1) - __ldg(a.seq.cu + j);
+        longer += (lj > li || (lj == li && j < i)) ? 1 : 0;
+      }
+      if (longer == rank) *pick = i;  // exactly one i: the order is strict
+    }
+    __syncthreads();
+    n = *pick;
+  }
 
   int start, end;
   bool ok = seq_ok(a.seq, n, start, end);
@@ -570,7 +595,9 @@ cudaError_t launch_one(const ScanArgs &a, const ScanMaps &maps, cudaStream_t str
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
   if (err != cudaSuccess) return err;
-  kern<<<dim3(a.seq.n_seqs, a.HV, a.dv / NS), kThreads, SM::kBytes, stream>>>(a, maps);
+  const long blocks = (long)a.seq.n_seqs * a.HV * (a.dv / NS);
+  if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
+  kern<<<(unsigned)blocks, kThreads, SM::kBytes, stream>>>(a, maps);
   return cudaGetLastError();
 }
 
