@@ -30,6 +30,30 @@ __device__ __forceinline__ bool seq_ok(const SeqInfo &s, int n, int &start,
   return start >= 0 && start <= end && end <= s.Ttot;
 }
 
+// Block order of the serial scans.  Blocks are launched in index order, and a
+// block runs one (sequence, value head, dv slice) chain from start to end, so
+// block b = rank * HV * slices + head * slices + slice, where for packed input
+// of up to kLptSeqs sequences the rank counts sequences by decreasing length
+// (ties by index): the longest chains start first and the short ones fill in
+// behind them (greedy longest-first list scheduling).  Otherwise rank =
+// sequence.  Every thread of the block calls this (it synchronises the
+// block); `pick` is one int of shared memory.
+constexpr int kLptSeqs = 64;
+__device__ __forceinline__ int scan_sequence(const SeqInfo &s, int rank, int *pick) {
+  if (!s.cu || s.n_seqs > kLptSeqs) return rank;
+  for (int i = threadIdx.x; i < s.n_seqs; i += blockDim.x) {
+    const int li = __ldg(s.cu + i + 1) - __ldg(s.cu + i);
+    int longer = 0;
+    for (int j = 0; j < s.n_seqs; j++) {
+      const int lj = __ldg(s.cu + j + 1) - __ldg(s.cu + j);
+      longer += (lj > li || (lj == li && j < i)) ? 1 : 0;
+    }
+    if (longer == rank) *pick = i;  // exactly one i: the order is strict
+  }
+  __syncthreads();
+  return *pick;
+}
+
 // ---------------------------------------------------------------------------
 // element conversion
 // ---------------------------------------------------------------------------

@@ -75,7 +75,11 @@ gdn_scan_kernel(const ScanArgs a) {
   float *DDs = smem + SM::kDD;
   float *Os = smem + SM::kO;
 
-  const int n = blockIdx.x, hv = blockIdx.y, col0 = blockIdx.z * NS;
+  // longest packed sequences first (scan_sequence)
+  __shared__ int lpt_pick;
+  const int n_slices = a.dv / NS;
+  const int hv = (blockIdx.x / n_slices) % a.HV, col0 = (blockIdx.x % n_slices) * NS;
+  const int n = scan_sequence(a.seq, blockIdx.x / (a.HV * n_slices), &lpt_pick);
   const int hq = hv / (a.HV / a.H);
   const int tid = threadIdx.x, warp = tid >> 5;
 
@@ -304,8 +308,9 @@ cudaError_t launch_one(const ScanArgs &a, cudaStream_t stream) {
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SM::kBytes);
   if (err != cudaSuccess) return err;
-  dim3 grid(a.seq.n_seqs, a.HV, a.dv / NS);
-  kern<<<grid, kScanThreads, SM::kBytes, stream>>>(a);
+  const long blocks = (long)a.seq.n_seqs * a.HV * (a.dv / NS);
+  if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
+  kern<<<(unsigned)blocks, kScanThreads, SM::kBytes, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -60,7 +60,6 @@ constexpr int kCoefWarp = 9;
 constexpr int kKqWarp0 = 10;      // warps 10-11
 constexpr int kKqThreads = 64;
 constexpr int kThreads = 384;
-constexpr int kLptSeqs = 64;      // packed sequences ranked by length per block
 constexpr int NS = kScanTcSlice;
 constexpr int NH = NS / 2;  // columns per chain thread
 static_assert(NS == 64, "one 128-byte swizzle atom per S / Y row");
@@ -129,31 +128,12 @@ gdn_scan_la_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SM::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SM::kMisc + 4);
 
-  // Blocks are launched in index order, and every block of a (sequence, value
-  // head, slice) runs that sequence's whole chain.  Block index = rank * HV *
-  // slices + head * slices + slice, and for packed input of up to kLptSeqs
-  // sequences the rank counts sequences by decreasing length (ties by index):
-  // the longest chains start first, so the short ones fill in behind them
-  // instead of a long chain starting last.
+  // longest packed sequences first (scan_sequence)
   const int n_slices = a.dv / NS;
   const int rank = blockIdx.x / (a.HV * n_slices);
   const int hv = (blockIdx.x / n_slices) % a.HV, col0 = (blockIdx.x % n_slices) * NS;
   const int hq = hv / (a.HV / a.H);
-  int n = rank;
-  if (a.seq.cu && a.seq.n_seqs <= kLptSeqs) {
-    int *pick = reinterpret_cast<int *>(sm + SM::kMisc + 8);
-    for (int i = tid; i < a.seq.n_seqs; i += kThreads) {
-      const int li = __ldg(a.seq.cu + i + 1) - __ldg(a.seq.cu + i);
-      int longer = 0;
-      for (int j = 0; j < a.seq.n_seqs; j++) {
-        const int lj = __ldg(a.seq.cu + j + 1) - __ldg(a.seq.cu + j);
-        longer += (lj > li || (lj == li && j < i)) ? 1 : 0;
-      }
-      if (longer == rank) *pick = i;  // exactly one i: the order is strict
-    }
-    __syncthreads();
-    n = *pick;
-  }
+  const int n = scan_sequence(a.seq, rank, reinterpret_cast<int *>(sm + SM::kMisc + 8));
 
   int start, end;
   bool ok = seq_ok(a.seq, n, start, end);

@@ -107,7 +107,11 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SM::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SM::kMisc + 4);
 
-  const int n = blockIdx.x, hv = blockIdx.y, col0 = blockIdx.z * NS;
+  // longest packed sequences first (scan_sequence)
+  const int n_slices = a.dv / NS;
+  const int hv = (blockIdx.x / n_slices) % a.HV, col0 = (blockIdx.x % n_slices) * NS;
+  const int n = scan_sequence(a.seq, blockIdx.x / (a.HV * n_slices),
+                              reinterpret_cast<int *>(sm + SM::kMisc + 8));
 
   int start, end;
   bool ok = seq_ok(a.seq, n, start, end);
@@ -407,7 +411,9 @@ cudaError_t launch_one(const ScanArgs &a, const ScanMaps &maps, cudaStream_t str
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
   if (err != cudaSuccess) return err;
-  kern<<<dim3(a.seq.n_seqs, a.HV, a.dv / NS), kThreads, SM::kBytes, stream>>>(a, maps);
+  const long blocks = (long)a.seq.n_seqs * a.HV * (a.dv / NS);
+  if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
+  kern<<<(unsigned)blocks, kThreads, SM::kBytes, stream>>>(a, maps);
   return cudaGetLastError();
 }
 
