@@ -29,8 +29,10 @@
  *  - Every pointer argument except `flags_out` is a DEVICE pointer.
  *  - Ownership: the caller allocates every buffer, workspace included; the
  *    library allocates no memory, keeps no per-call state and may be called
- *    from several host threads at once (one-time kernel attribute set-up is
- *    guarded internally).
+ *    from several host threads at once.  The one-time lookup of the driver's
+ *    tensor-map encoder is guarded internally; a kernel's shared-memory size
+ *    attribute is set at each launch, which the CUDA runtime makes safe from
+ *    several threads.
  *  - Asynchrony: work is enqueued on `stream` (NULL = legacy default stream)
  *    and the call returns without synchronising.  Errors of the launch itself
  *    are returned as GDN_ERR_CUDA; faults during execution surface at the
