@@ -439,6 +439,28 @@ gdn_status gdn_rmsnorm_gated_fwd(const void *x, const void *z, const float *weig
   return rownorm(1, x, z, weight, y, rows, dim, eps, dtype, stream);
 }
 
+gdn_status gdn_state_combine(const float *M, const float *S_in, const float *S_seg,
+                             float *S_out, int n_seqs, int HV, int dk, int dv,
+                             gdn_stream_t stream) {
+  if (n_seqs < 0 || HV <= 0 || dk <= 0 || dv <= 0) return GDN_ERR_INVALID_ARG;
+  if (dk > 1024 || dv > 1024) return GDN_ERR_UNSUPPORTED;
+  const long n_states = (long)n_seqs * HV;
+  if (n_states > 0 && (!M || !S_in || !S_seg || !S_out)) return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {M, S_in, S_seg, S_out};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+  const size_t n_m = (size_t)n_states * dk * dk * 4, n_s = (size_t)n_states * dk * dv * 4;
+  // S_out may be S_seg itself; it overlaps nothing else
+  if (overlap(S_out, n_s, M, n_m) || overlap(S_out, n_s, S_in, n_s)) return GDN_ERR_INVALID_ARG;
+  if (S_out != S_seg && overlap(S_out, n_s, S_seg, n_s)) return GDN_ERR_INVALID_ARG;
+  gdn::TransferArgs ta;
+  ta.M = M; ta.S_in = S_in; ta.S_seg = S_seg; ta.S_out = S_out;
+  ta.n_states = n_states; ta.dk = dk; ta.dv = dv;
+  if (gdn::launch_state_combine(ta, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
 gdn_status gdn_read_device_flags(const void *workspace, uint32_t *flags_out,
                                  gdn_stream_t stream_) {
   if (!workspace || !flags_out) return GDN_ERR_INVALID_ARG;

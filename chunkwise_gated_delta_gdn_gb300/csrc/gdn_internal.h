@@ -99,6 +99,15 @@ struct RowNormArgs {
   float eps;
 };
 
+// Composition of a segment's state transfer (gdn_transfer.cu):
+// S_out = M S_in + S_seg per (state, value head); n_states = sequences x heads.
+struct TransferArgs {
+  const float *M, *S_in, *S_seg;
+  float *S_out;
+  long n_states;
+  int dk, dv;
+};
+
 // Status-word bits (same values as GDN_FLAG_* in include/gdn.h).
 constexpr uint32_t kFlagPositiveGate = 1u << 0;
 constexpr uint32_t kFlagNonfinite = 1u << 1;
@@ -139,6 +148,8 @@ cudaError_t launch_conv1d(const ConvArgs &a, int width, int activation, int dtyp
                           cudaStream_t stream);
 cudaError_t launch_rownorm(const RowNormArgs &a, int dim, int kind, int dtype,
                            cudaStream_t stream);
+// S_out = M S_in + S_seg, per state
+cudaError_t launch_state_combine(const TransferArgs &a, cudaStream_t stream);
 // token-serial form; dv a multiple of 32
 cudaError_t launch_recurrent(const RecurrentArgs &a, int dk, int dtype, int gate,
                              cudaStream_t stream);

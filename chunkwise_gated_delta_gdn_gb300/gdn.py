@@ -41,7 +41,8 @@ GDN_FLAG_TIMEOUT = 1 << 3
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_chunk_fwd_workspace_bytes",
             "gdn_chunk_fwd", "gdn_chunk_fwd_prep", "gdn_chunk_fwd_scan",
             "gdn_chunk_fwd_noalloc", "gdn_recurrent_fwd", "gdn_causal_conv1d_fwd",
-            "gdn_l2norm_fwd", "gdn_rmsnorm_gated_fwd", "gdn_read_device_flags")
+            "gdn_l2norm_fwd", "gdn_rmsnorm_gated_fwd", "gdn_state_combine",
+            "gdn_read_device_flags")
 
 _lock = threading.Lock()
 _lib = None
@@ -96,6 +97,8 @@ def load(path: Optional[str] = None):
         lib.gdn_l2norm_fwd.restype = i32
         lib.gdn_rmsnorm_gated_fwd.argtypes = [vp, vp, vp, vp, i64, i32, f32, i32, vp]
         lib.gdn_rmsnorm_gated_fwd.restype = i32
+        lib.gdn_state_combine.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp]
+        lib.gdn_state_combine.restype = i32
         lib.gdn_read_device_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gdn_read_device_flags.restype = i32
         _lib = lib
@@ -358,6 +361,31 @@ def gdn_rmsnorm_gated_fwd(x: torch.Tensor, weight: torch.Tensor, z: Optional[tor
     if status != GDN_OK:
         raise GdnError(status, "gdn_rmsnorm_gated_fwd")
     return y
+
+
+def gdn_state_combine(M: torch.Tensor, S_in: torch.Tensor, S_seg: torch.Tensor, *,
+                      out: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """S_out = M S_in + S_seg per (state, value head): M ``[N, HV, dk, dk]``,
+    S_in and S_seg ``[N, HV, dk, dv]``, fp32 (``out=S_seg`` composes in place)."""
+    lib = load()
+    dev = M.device
+    for name, t in (("M", M), ("S_in", S_in), ("S_seg", S_seg), ("out", out)):
+        _check(t, name, dev)
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    N, HV, dk, dv = S_in.shape
+    if M.shape != (N, HV, dk, dk) or S_seg.shape != S_in.shape:
+        raise ValueError("M [N, HV, dk, dk] and S_seg [N, HV, dk, dv] must match S_in")
+    if out is None:
+        out = torch.empty_like(S_seg)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    status = lib.gdn_state_combine(_ptr(M), _ptr(S_in), _ptr(S_seg), _ptr(out), N, HV, dk, dv,
+                                   ctypes.c_void_p(stream.cuda_stream))
+    if status != GDN_OK:
+        raise GdnError(status, "gdn_state_combine")
+    return out
 
 
 def gdn_read_device_flags(workspace: torch.Tensor,

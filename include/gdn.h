@@ -284,6 +284,24 @@ GDN_API gdn_status gdn_rmsnorm_gated_fwd(const void *x, const void *z, const flo
                                          gdn_stream_t stream);
 
 /*
+ * gdn_state_combine -- compose a segment's state transfer.  Over any run of a
+ * sequence's tokens the recurrence maps its entering state affinely,
+ * S_out = M S_in + S_seg, with S_seg the state the run leaves from a zero
+ * start (gdn_chunk_fwd with h0 = NULL) and M the state it leaves from the
+ * identity with all values zero (gdn_chunk_fwd with v = 0, dv = dk, h0 = I).
+ * A sequence split into segments on several GPUs exchanges (M, S_seg) per
+ * segment and composes them with this product (the state-transfer exchange
+ * for sequences longer than one GPU's share; logismos issue #46, "Remaining
+ * work", later continuation).  Per state n < n_seqs and value head:
+ *     S_out = M S_in + S_seg,  M [n_seqs, HV, dk, dk], the others
+ *     [n_seqs, HV, dk, dv], all fp32, device pointers, 16-byte aligned.
+ * S_out may be S_seg itself; it must not overlap M or S_in.  dk, dv <= 1024.
+ */
+GDN_API gdn_status gdn_state_combine(const float *M, const float *S_in, const float *S_seg,
+                                     float *S_out, int n_seqs, int HV, int dk, int dv,
+                                     gdn_stream_t stream);
+
+/*
  * Copy the device status word of `workspace` to *flags_out (host pointer)
  * after all work queued on `stream` so far has finished (synchronises the
  * stream).  Returns GDN_ERR_INVALID_ARG for NULL arguments and GDN_ERR_CUDA

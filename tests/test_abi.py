@@ -220,3 +220,20 @@ def test_rownorm_refusals(lib, entry, kw, status):
 def test_rmsnorm_needs_its_weight(lib):
     assert lib.gdn_rmsnorm_gated_fwd(addr(0), None, None, addr(3), 10, 128, 1e-6, 1,
                                      None) == gdn.GDN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(M=None), gdn.GDN_ERR_INVALID_ARG),
+    (dict(HV=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(n=-1), gdn.GDN_ERR_INVALID_ARG),
+    (dict(dk=2048), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(S_out=addr(0)), gdn.GDN_ERR_INVALID_ARG),     # S_out aliases M
+    (dict(S_out=addr(1)), gdn.GDN_ERR_INVALID_ARG),     # S_out aliases S_in
+    (dict(S_out=ctypes.c_void_p(BASE + 2 * STRIDE + 64)), gdn.GDN_ERR_INVALID_ARG),  # partial
+    (dict(M=ctypes.c_void_p(BASE + 4)), gdn.GDN_ERR_INVALID_ARG),
+])
+def test_state_combine_refusals(lib, kw, status):
+    a = dict(M=addr(0), S_in=addr(1), S_seg=addr(2), S_out=addr(3), n=1, HV=4, dk=128, dv=128)
+    a.update(kw)
+    assert lib.gdn_state_combine(a["M"], a["S_in"], a["S_seg"], a["S_out"], a["n"], a["HV"],
+                                 a["dk"], a["dv"], None) == status

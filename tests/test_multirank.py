@@ -72,3 +72,50 @@ def test_several_gpus_without_torchrun_is_refused():
                        capture_output=True, text=True, env=env, cwd=ROOT, timeout=120)
     assert r.returncode != 0
     assert "torchrun" in (r.stderr + r.stdout)
+
+
+def _exchange_main(rank, world, port, Ms, Ss, h0, out):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    from chunkwise_gated_delta_gdn_gb300 import seqsplit
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        s_in = seqsplit.exchange_and_compose(Ms[rank], Ss[rank], h0,
+                                             combine=lambda M, S, Sg: M @ S + Sg)
+        out.put((rank, s_in))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_three_ranks_compose_the_state_transfers_in_rank_order():
+    """Each rank's entering state is the composition of the transfers of the
+    ranks before it (the sequence-split exchange), checked against a plain
+    sequential fold."""
+    import torch
+
+    gen = torch.Generator().manual_seed(5)
+    world = 3
+    Ms = [torch.randn((1, 2, 4, 4), generator=gen, dtype=torch.float64) * 0.5 for _ in range(world)]
+    Ss = [torch.randn((1, 2, 4, 3), generator=gen, dtype=torch.float64) for _ in range(world)]
+    h0 = torch.randn((1, 2, 4, 3), generator=gen, dtype=torch.float64)
+    expect, s = [], h0
+    for p in range(world):
+        expect.append(s)
+        s = Ms[p] @ s + Ss[p]
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_exchange_main, args=(r, world, port, Ms, Ss, h0, out))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    got = dict(out.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in range(world):
+        assert torch.allclose(got[r], expect[r], atol=1e-12), r
