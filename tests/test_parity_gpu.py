@@ -140,6 +140,36 @@ def test_continuation_on_device():
     assert_close(h2.cpu(), hT.cpu().double(), "bf16", "continued hT")
 
 
+@pytest.mark.parametrize("name, over", [
+    ("gdn_bf16_t4096", dict(T=300, H=2, HV=4)),            # bf16 scalar gate
+    ("kda_bf16_b2_t8192", dict(T=150, H=2, HV=4)),         # bf16 per-key gate
+    ("gdn_fp32_t256", dict(T=200)),                        # fp32
+    ("gdn_varlen_t131072", dict(T=700, H=2, HV=4)),        # packed sequences
+])
+def test_halves_equal_one_call_bitwise(name, over):
+    """The prep and scan halves called one after the other (as separate
+    entries, on the same workspace) give the bits of the one-call entry:
+    they launch the same kernels (split and fused paths sharing one scan
+    body are equal bit for bit: ROCm/rocm-libraries PR #11223,
+    "Correctness")."""
+    c = synth.case(name, **over)
+    d = to_dev(synth.make_inputs(c))
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    kw = dict(scale=c.scale, chunk=c.chunk, cu_seqlens=d["cu_seqlens"])
+    o1, h1 = gdn.gdn_chunk_fwd(*args, **kw)
+    gate_mode = gdn.GDN_GATE_PER_KEY if d["g"].dim() == 4 else gdn.GDN_GATE_SCALAR
+    nbytes = gdn.gdn_chunk_fwd_workspace_bytes(
+        d["q"].shape[0], d["q"].shape[1], c.H, c.HV, c.dk, c.dv, c.chunk, gate_mode,
+        h1.shape[0], gdn._dtype_code(d["q"].dtype))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    o2 = torch.empty_like(o1)
+    h2 = torch.empty_like(h1)
+    gdn.gdn_chunk_fwd_prep(*args, workspace=ws, o=o2, hT=h2, **kw)
+    gdn.gdn_chunk_fwd_scan(*args, workspace=ws, o=o2, hT=h2, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
 def test_deterministic():
     c = synth.case("kda_bf16_b2_t8192", T=200, H=2, HV=4)
     x = synth.make_inputs(c)
