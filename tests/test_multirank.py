@@ -1,7 +1,11 @@
-"""The multi-rank host logic of bench.py, run as world-size-2 gloo ranks on
-the CPU: every rank gets the slowest rank's step time, and the reported value
-is the units all ranks processed over that time (replicas, weak scaling; the
-path has no exchange step, so no collective touches the data)."""
+"""Multi-rank host logic, run as gloo ranks on the CPU.
+
+* bench.py: every rank gets the slowest rank's step time, and the reported
+  value is the units all ranks processed over that time (independent
+  sequences per rank, weak scaling: no collective touches the data).
+* The sequence split: one sequence cut into per-rank segments needs one
+  exchange, an all-gather of the segments' state transfers, after which each
+  rank composes its own entering state."""
 from __future__ import annotations
 
 import os
