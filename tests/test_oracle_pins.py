@@ -306,6 +306,35 @@ def test_joint_linearity_in_state_and_values(gate_mode):
     np.testing.assert_allclose(c[1], 2.0 * a[1] - 3.0 * b[1], atol=1e-11)
 
 
+@pytest.mark.parametrize("gate_mode", [0, 1])
+@pytest.mark.parametrize("fn", ["token_serial", "chunked"])
+def test_state_transfer_is_product_of_token_maps(gate_mode, fn):
+    """The reading the sequence split rests on: over a segment the state maps
+    affinely, S_out = M S_in + S_seg.  A pass with every value zero and the
+    identity as initial state (dv = dk) must leave M, the product of the
+    per-token maps A_t = (I - beta_t k_t k_t^T) diag(a_t), formed here one
+    plain matrix at a time; a pass from a zero state leaves S_seg; any other
+    entering state must then give M S_in + S_seg (logismos issue #46,
+    "Remaining work": later continuation)."""
+    T, dk, dv = 37, 8, 6
+    q, k, v, g, beta, h0 = rand_case(T, dk=dk, dv=dv, gate_mode=gate_mode, seed=21)
+    f = oracle.token_serial if fn == "token_serial" else \
+        (lambda *a: oracle.chunked(*a, chunk=16))  # three chunks, ragged tail
+    eye = np.broadcast_to(np.eye(dk), (1, 4, dk, dk)).copy()
+    v0 = np.zeros((T, 4, dk))
+    _, M = run(q, k, v0, g, beta, eye, gate_mode=gate_mode, fn=f)
+    _, S_seg = run(q, k, v, g, beta, None, gate_mode=gate_mode, fn=f)
+    _, S_out = run(q, k, v, g, beta, h0, gate_mode=gate_mode, fn=f)
+    for hv in range(4):
+        P = np.eye(dk)
+        for t in range(T):
+            kt = k[t, hv // 2]
+            a = np.exp(g[t, hv]) * np.ones(dk)
+            P = (np.eye(dk) - beta[t, hv] * np.outer(kt, kt)) @ np.diag(a) @ P
+        np.testing.assert_allclose(M[0, hv], P, atol=1e-12)
+        np.testing.assert_allclose(S_out[0, hv], P @ h0[0, hv] + S_seg[0, hv], atol=1e-12)
+
+
 def test_state_norm_bound():
     """With |k| = 1 and 0 <= beta <= 1 the transition (I - beta k k^T) diag(a)
     is a contraction, so ||S_T||_F <= ||h0||_F + sum_t beta_t ||v_t||."""
