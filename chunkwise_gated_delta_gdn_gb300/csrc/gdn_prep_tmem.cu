@@ -16,9 +16,9 @@
 //          exp(b_r - b_o) exp(b_o - b_s) with o the block's first row (both
 //          factors <= 1 for non-positive gates: nothing overflows)
 //   T    = (I + A)^-1 blocked as in ROCm/rocm-libraries PR #11223 ("Levers"
-//          3): each 32 x 32 diagonal block by forward substitution in registers
-//          (one warp per block, one thread per column), then the off-diagonal
-//          block T10 = -T11 (A10 T00); fp32 on the CUDA cores throughout
+//          3): each 16 x 16 diagonal block by fp32 forward substitution in
+//          registers (one lane per column), then the 32 x 32 and 64 x 64 levels
+//          T10 = -T11 (A10 T00) as split-tf32 mma.sync products (fp32-class)
 //   P1   = K^T (D T)         the key tile read MN-major, D = diag(exp(b_last - b_s))
 //   AqkT = Aqk T
 //   E    = K_next P1         (fp16 P1 as the B operand; zero for the last chunk
