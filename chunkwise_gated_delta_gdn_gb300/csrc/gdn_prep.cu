@@ -1,4 +1,4 @@
-// gdn_prep.cu -- the state-independent chunk-prep kernel.
+// gdn_prep.cu -- the state-independent chunk-prep kernel of the fp32 path.
 //
 // One CTA per (chunk slot, value head).  For the C-row chunk it forms
 //   b      cumulative natural-log gates (per key channel for KDA)
@@ -13,7 +13,7 @@
 // cheap elementwise products and are formed by the scan kernel when it needs
 // them, so they never cross HBM.
 //
-// GDN: the Gram K K^T and Q K^T run on the tensor cores (exact bf16 inputs,
+// GDN: the Gram K K^T and Q K^T run on the tensor cores (split-bf16 operands,
 // fp32 accumulation); the scalar pairwise decay exp(b_r - b_s) is applied per
 // element afterwards, never factored, and only for s <= r, so no exponent is
 // positive.  KDA: the per-channel decay sits inside the contraction; each
@@ -276,10 +276,10 @@ cudaError_t launch_one(const PrepArgs &a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Instantiated for fp32 inputs only: bf16 inputs run the tensor-memory
+// kernels, so the bf16 form of this kernel is not compiled.
 template <int C, int DK>
 cudaError_t dispatch_dt_gate(const PrepArgs &a, int dtype, int gate, cudaStream_t s) {
-  if (dtype == 1 && gate == 0) return launch_one<C, DK, true, 0>(a, s);
-  if (dtype == 1 && gate == 1) return launch_one<C, DK, true, 1>(a, s);
   if (dtype == 0 && gate == 0) return launch_one<C, DK, false, 0>(a, s);
   if (dtype == 0 && gate == 1) return launch_one<C, DK, false, 1>(a, s);
   return cudaErrorInvalidValue;

@@ -1,4 +1,4 @@
-// gdn_scan.cu -- the serial-across-chunks scan kernel.
+// gdn_scan.cu -- the serial-across-chunks scan kernel of the fp32 path.
 //
 // One CTA per (sequence, value head, 32-column slice of dv); the slice split
 // manufactures parallelism that a (sequence, head) grid lacks (ROCm/rocm-
@@ -17,8 +17,9 @@
 //
 // (b_last: cumulative gate at the chunk's last row; scalar per row for GDN,
 // per key channel for KDA.)  Every product runs on the tensor cores in split
-// bf16 (16-bit mantissa operands, fp32 accumulation); raw bf16 q/k of GDN are
-// exact operands and skip their low halves.
+// bf16 (16-bit mantissa operands, fp32 accumulation).  The kernel is written
+// for either input type (raw bf16 q/k would be exact operands and skip their
+// low halves), but only its fp32 form is compiled.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -314,10 +315,10 @@ cudaError_t launch_one(const ScanArgs &a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Instantiated for fp32 inputs only: bf16 inputs run the tensor-memory
+// kernels, so the bf16 form of this kernel is not compiled.
 template <int C, int DK>
 cudaError_t dispatch_dt_gate(const ScanArgs &a, int dtype, int gate, cudaStream_t s) {
-  if (dtype == 1 && gate == 0) return launch_one<C, DK, true, 0>(a, s);
-  if (dtype == 1 && gate == 1) return launch_one<C, DK, true, 1>(a, s);
   if (dtype == 0 && gate == 0) return launch_one<C, DK, false, 0>(a, s);
   if (dtype == 0 && gate == 1) return launch_one<C, DK, false, 1>(a, s);
   return cudaErrorInvalidValue;
