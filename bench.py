@@ -232,6 +232,18 @@ def oracle_sample(c, x, n_tokens):
     return time.perf_counter() - t, Bq * n_tokens
 
 
+def oracle_sample_text(c0, x, n):
+    """What oracle_sample processed, from the tokens it reports."""
+    if x["cu_seqlens"] is not None:
+        where = f"the first {n} tokens of the first packed sequence"
+    elif x["q"].shape[0] == 1:
+        where = f"the first {n} tokens"
+    else:
+        rows = x["q"].shape[0]
+        where = f"the first {n // rows} tokens of each of the {rows} batch rows ({n} tokens)"
+    return f"fp64 token-serial oracle on {where} (all {c0.HV} value heads) of {c0.name}"
+
+
 def calibrate_oracle(c, x, target_s):
     sec, n = oracle_sample(c, x, 64)
     per_token = sec / n
@@ -473,8 +485,7 @@ def main():
         n_tok = calibrate_oracle(wl, x, args.cpu_seconds)
         sec, n = oracle_sample(wl, x, n_tok)
         cpu = {"value": n / sec, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-               "sample": f"fp64 token-serial oracle on the first {n} tokens (all {c0.HV} value "
-                         f"heads) of {c0.name}, {sec:.1f} s"}
+               "sample": f"{oracle_sample_text(c0, x, n)}, {sec:.1f} s"}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -830,7 +841,8 @@ def run_reference(args, rank, world, c0, wl, config):
 
         sec, n_s = sample(64)
         n_tok = int(min(c0.T, max(64, per_step_s / max(sec / n_s, 1e-9))))
-        what = f"the numpy fp64 oracle of the three operations on the first {n_tok} tokens"
+        describe = lambda n: (f"the numpy fp64 oracle of the three operations on the first "
+                              f"{n} tokens of {c0.name}")
         cores = 1
     else:
         x = synth.make_inputs(c0)
@@ -839,7 +851,7 @@ def run_reference(args, rank, world, c0, wl, config):
         def sample(n_s):
             return oracle_sample(wl, x, n_s)
 
-        what = f"fp64 token-serial oracle on the first {n_tok} tokens (all {c0.HV} value heads)"
+        describe = lambda n: oracle_sample_text(c0, x, n)
         cores = oracle.num_threads()
     for _ in range(args.warmup):
         sample(n_tok)
@@ -855,7 +867,7 @@ def run_reference(args, rank, world, c0, wl, config):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; no dataset)",
             "config": config,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"each step: {what} of {c0.name}"},
+                             "sample": f"each step: {describe(n)}"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
