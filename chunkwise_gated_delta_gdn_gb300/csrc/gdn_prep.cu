@@ -46,6 +46,10 @@ struct PrepSmem {
   static constexpr int kMeta = kR + 16 * 17;       // t0, L, valid
   static constexpr int kFloats = kMeta + 4;
   static constexpr size_t kBytes = sizeof(float) * kFloats;
+  static_assert(C == 32 || C == 64, "the chunk length C is 32 or 64");
+  static_assert(DK == 64 || DK == 128, "the key width dk is 64 or 128");
+  static_assert(GATE == 0 || GATE == 1, "scalar (GDN) or per-key (KDA) gate");
+  static_assert(kBytes <= 227 * 1024, "one CTA's shared memory fits an SM");
 };
 
 template <int C, int DK, bool BF16, int GATE>
