@@ -42,7 +42,7 @@ EXPORTED = ("gdn_version", "gdn_status_string", "gdn_chunk_fwd_workspace_bytes",
             "gdn_chunk_fwd", "gdn_chunk_fwd_prep", "gdn_chunk_fwd_scan",
             "gdn_chunk_fwd_noalloc", "gdn_recurrent_fwd", "gdn_causal_conv1d_fwd",
             "gdn_l2norm_fwd", "gdn_rmsnorm_gated_fwd", "gdn_state_combine",
-            "gdn_read_device_flags")
+            "gdn_selftest_wait", "gdn_read_device_flags")
 
 _lock = threading.Lock()
 _lib = None
@@ -99,6 +99,8 @@ def load(path: Optional[str] = None):
         lib.gdn_rmsnorm_gated_fwd.restype = i32
         lib.gdn_state_combine.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp]
         lib.gdn_state_combine.restype = i32
+        lib.gdn_selftest_wait.argtypes = [vp, ctypes.c_longlong, i32, vp]
+        lib.gdn_selftest_wait.restype = i32
         lib.gdn_read_device_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gdn_read_device_flags.restype = i32
         _lib = lib
@@ -386,6 +388,24 @@ def gdn_state_combine(M: torch.Tensor, S_in: torch.Tensor, S_seg: torch.Tensor, 
     if status != GDN_OK:
         raise GdnError(status, "gdn_state_combine")
     return out
+
+
+def gdn_selftest_wait(flags: torch.Tensor, budget_cycles: int, complete: bool, *,
+                      stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Run the bounded-wait self-test into ``flags`` (a uint32-sized int32
+    tensor on the device): a wait on a barrier that never completes
+    (``complete=False``) must leave GDN_FLAG_TIMEOUT there; one that completes
+    must leave 0.  Read it back with :func:`gdn_read_device_flags`."""
+    lib = load()
+    _check(flags, "flags", flags.device)
+    if flags.dtype != torch.int32 or flags.numel() < 1:
+        raise TypeError("flags must be an int32 tensor of at least one element")
+    if stream is None:
+        stream = torch.cuda.current_stream(flags.device)
+    status = lib.gdn_selftest_wait(_ptr(flags), int(budget_cycles), int(bool(complete)),
+                                   ctypes.c_void_p(stream.cuda_stream))
+    if status != GDN_OK:
+        raise GdnError(status, "gdn_selftest_wait")
 
 
 def gdn_read_device_flags(workspace: torch.Tensor,

@@ -302,6 +302,23 @@ GDN_API gdn_status gdn_state_combine(const float *M, const float *S_in, const fl
                                      gdn_stream_t stream);
 
 /*
+ * gdn_selftest_wait -- exercise the bounded wait that every mbarrier wait of
+ * the tensor-core kernels uses, with no fault and no hang.  Those waits give
+ * up after a clock budget (about two seconds), set GDN_FLAG_TIMEOUT and let
+ * the kernel finish, so that a completion that never comes ends as a status,
+ * not a hung GPU.  This call clears the uint32 at `flags` (DEVICE pointer,
+ * 4-byte aligned), then runs one 32-thread block that waits, with a budget of
+ * `budget_cycles` SM clock cycles (1 .. 4e9), on a barrier of its own:
+ * complete = 0: nothing arrives, every wait runs out and *flags becomes
+ * GDN_FLAG_TIMEOUT; complete = 1: the barrier completes first and *flags stays
+ * 0.  Read the word back with gdn_read_device_flags(flags, ...).
+ * (Failure detection the pages ask for in spirit -- invalid work is refused
+ * before publication, logismos issue #46; they describe no such entry point.)
+ */
+GDN_API gdn_status gdn_selftest_wait(uint32_t *flags, long long budget_cycles, int complete,
+                                     gdn_stream_t stream);
+
+/*
  * Copy the device status word of `workspace` to *flags_out (host pointer)
  * after all work queued on `stream` so far has finished (synchronises the
  * stream).  Returns GDN_ERR_INVALID_ARG for NULL arguments and GDN_ERR_CUDA

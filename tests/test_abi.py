@@ -237,3 +237,18 @@ def test_state_combine_refusals(lib, kw, status):
     a.update(kw)
     assert lib.gdn_state_combine(a["M"], a["S_in"], a["S_seg"], a["S_out"], a["n"], a["HV"],
                                  a["dk"], a["dv"], None) == status
+
+
+@pytest.mark.parametrize("kw", [
+    dict(flags=None),
+    dict(flags=ctypes.c_void_p(BASE + 2)),   # not 4-byte aligned
+    dict(budget=0),
+    dict(budget=-5),
+    dict(budget=4000000001),
+    dict(complete=2),
+])
+def test_selftest_wait_refusals(lib, kw):
+    a = dict(flags=addr(0), budget=1000, complete=0)
+    a.update(kw)
+    assert lib.gdn_selftest_wait(a["flags"], a["budget"], a["complete"], None) == \
+        gdn.GDN_ERR_INVALID_ARG
