@@ -113,6 +113,7 @@ constexpr uint32_t kFlagPositiveGate = 1u << 0;
 constexpr uint32_t kFlagNonfinite = 1u << 1;
 constexpr uint32_t kFlagBadSeqlens = 1u << 2;
 constexpr uint32_t kFlagTimeout = 1u << 3;
+constexpr uint32_t kFlagLaunchConfig = 1u << 4;
 
 // Launchers; return cudaErrorInvalidValue for an uncompiled combination.
 // dtype: 0 = fp32, 1 = bf16.  gate: 0 = scalar (GDN), 1 = per key (KDA).

@@ -94,7 +94,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   unsigned char *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (sm - smem_raw > SM::kSlack) {  // dynamic shared memory not aligned as needed
-    if (tid == 0) atomicOr(a.flags, kFlagTimeout);
+    if (tid == 0) atomicOr(a.flags, kFlagLaunchConfig);
     return;
   }
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::kBar);

@@ -36,6 +36,7 @@ GDN_FLAG_POSITIVE_GATE = 1 << 0
 GDN_FLAG_NONFINITE = 1 << 1
 GDN_FLAG_BAD_SEQLENS = 1 << 2
 GDN_FLAG_TIMEOUT = 1 << 3
+GDN_FLAG_LAUNCH_CONFIG = 1 << 4
 
 # every symbol include/gdn.h declares
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_chunk_fwd_workspace_bytes",

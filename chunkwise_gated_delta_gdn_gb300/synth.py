@@ -210,17 +210,18 @@ def make_prepost_inputs(c: Case, width: int = 4) -> dict:
 
 def sweep_cases() -> list[Case]:
     """The parity sweep: T in {1, 37, 64, 65, 200, 4099} x gate lower bound in
-    {-0.05, -1, -5} x {scalar gate, per-key gate}, small head counts (the T
-    sweep and decay modes of stratat pull #1296, "The parity discipline"; the
-    gate range to -5 of PR #11223, "Correctness")."""
+    {-0.05, -1, -5} x {scalar gate, per-key gate} x {bf16, fp32} inputs, small
+    head counts (the T sweep and decay modes of stratat pull #1296, "The parity
+    discipline"; the gate range to -5 of PR #11223, "Correctness")."""
     out = []
-    for gate_mode in (GATE_SCALAR, GATE_PER_KEY):
-        for T in (1, 37, 64, 65, 200, 4099):
-            for low in (-0.05, -1.0, -5.0):
-                chunk = 64 if gate_mode == GATE_SCALAR else 32
-                out.append(Case(f"sweep_m{gate_mode}_T{T}_L{low}", B=1, T=T,
-                                H=2, HV=4, dk=128, dv=128, chunk=chunk,
-                                dtype=torch.bfloat16, gate_mode=gate_mode,
-                                gate_dist="uniform", gate_low=low, h0_std=0.1,
-                                seed=T))
+    for dtype, tag in ((torch.bfloat16, "bf16"), (torch.float32, "f32")):
+        for gate_mode in (GATE_SCALAR, GATE_PER_KEY):
+            for T in (1, 37, 64, 65, 200, 4099):
+                for low in (-0.05, -1.0, -5.0):
+                    chunk = 64 if gate_mode == GATE_SCALAR else 32
+                    out.append(Case(f"sweep_{tag}_m{gate_mode}_T{T}_L{low}", B=1, T=T,
+                                    H=2, HV=4, dk=128, dv=128, chunk=chunk,
+                                    dtype=dtype, gate_mode=gate_mode,
+                                    gate_dist="uniform", gate_low=low, h0_std=0.1,
+                                    seed=T))
     return out

@@ -90,8 +90,12 @@ enum {
   GDN_FLAG_NONFINITE = 1u << 1,     /* a non-finite value was written to o/hT */
   GDN_FLAG_BAD_SEQLENS = 1u << 2,   /* cu_seqlens not 0 = c0 <= c1 <= .. = T;
                                        affected sequences were skipped */
-  GDN_FLAG_TIMEOUT = 1u << 3        /* an internal wait ran out of its time
+  GDN_FLAG_TIMEOUT = 1u << 3,       /* an internal wait ran out of its time
                                        budget; the results are not valid */
+  GDN_FLAG_LAUNCH_CONFIG = 1u << 4  /* a kernel received dynamic shared memory
+                                       without the alignment its operand
+                                       images need and did no work; the
+                                       results are not valid */
 };
 
 /* Library version, major*10000 + minor*100 + patch. */
@@ -194,7 +198,12 @@ GDN_API gdn_status gdn_chunk_fwd_scan(const void *q, const void *k, const void *
  * that address up (with the device current); make that first call before any
  * stream capture.  All calls on a device share the one array: calls that
  * overlap on the GPU race and must be serialised by the caller.  The device
- * status word of these calls lives in that array and is not exposed.
+ * status word of these calls lives in that array and is not exposed, so what
+ * the kernels find on the device (a wait that ran out, malformed cu_seqlens,
+ * a non-finite result, a positive log-gate) cannot be detected through this
+ * entry point: the call still returns GDN_OK.  A caller that needs that
+ * status uses gdn_chunk_fwd with a workspace of its own and reads it with
+ * gdn_read_device_flags.
  */
 GDN_API gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                  const float *g, const float *beta,

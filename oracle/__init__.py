@@ -36,25 +36,33 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdn_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libgdn_oracle.so")
+# negative controls: deliberately wrong copies of the token walk, a library of
+# their own so that the oracle's walk carries no switch
+_PLANTED_SRC = os.path.join(_HERE, "planted_walk.c")
+_PLANTED_PATH = os.path.join(_BUILD_DIR, "libgdn_planted.so")
 _lock = threading.Lock()
 _lib = None
+_planted_lib = None
 
 GATE_SCALAR = 0  # GDN: one log-gate per (token, value head)
 GATE_PER_KEY = 1  # KDA: one log-gate per (token, value head, key channel)
 
 
+def _compile(src: str, out: str, force: bool, openmp: bool) -> str:
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(out)) or os.path.getmtime(out) < os.path.getmtime(src)
+    if force or stale:
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O3", "-ffp-contract=off", *(["-fopenmp"] if openmp else []),
+               "-fPIC", "-shared", "-std=c11", "-Wall", "-o", tmp, src, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc into ``oracle/_build``; returns the .so path."""
-    os.makedirs(_BUILD_DIR, exist_ok=True)
-    stale = (not os.path.exists(_LIB_PATH)) or (
-        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
-    if force or stale:
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O3", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
-               "-std=c11", "-Wall", "-o", tmp, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    return _compile(_SRC, _LIB_PATH, force, openmp=True)
 
 
 def _load():
@@ -70,8 +78,6 @@ def _load():
                       ctypes.c_double, ctypes.c_int]
             lib.gdn_oracle_token_serial.argtypes = common
             lib.gdn_oracle_token_serial.restype = ctypes.c_int
-            lib.gdn_oracle_token_serial_planted.argtypes = common + [ctypes.c_int]
-            lib.gdn_oracle_token_serial_planted.restype = ctypes.c_int
             lib.gdn_oracle_chunked.argtypes = common + [ctypes.c_int]
             lib.gdn_oracle_chunked.restype = ctypes.c_int
             lib.gdn_oracle_num_threads.argtypes = []
@@ -115,8 +121,23 @@ def pack_batched(q, k, v, g, beta):
     return (*flat, cu)
 
 
-def _run(entry, q, k, v, g, beta, h0, cu_seqlens, scale, gate_mode, extra=()):
-    lib = _load()
+def _load_planted():
+    global _planted_lib
+    with _lock:
+        if _planted_lib is None:
+            lib = ctypes.CDLL(_compile(_PLANTED_SRC, _PLANTED_PATH, False, openmp=False))
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.gdn_planted_token_serial.argtypes = [
+                dp, dp, dp, dp, dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                ctypes.c_int, ctypes.c_int]
+            lib.gdn_planted_token_serial.restype = ctypes.c_int
+            _planted_lib = lib
+    return _planted_lib
+
+
+def _run(entry, q, k, v, g, beta, h0, cu_seqlens, scale, gate_mode, extra=(), lib=None):
+    lib = lib or _load()
     q, k, v, g, beta, h0 = (_f64(x) for x in (q, k, v, g, beta, h0))
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
     Ttot, H, dk = q.shape
@@ -150,9 +171,10 @@ def token_serial(q, k, v, g, beta, h0, cu_seqlens, scale, gate_mode=GATE_SCALAR)
 
 def token_serial_planted(q, k, v, g, beta, h0, cu_seqlens, scale, gate_mode,
                          planted):
-    """The token walk with one planted mistake (negative controls only)."""
-    return _run("gdn_oracle_token_serial_planted", q, k, v, g, beta, h0,
-                cu_seqlens, scale, gate_mode, (int(planted),))
+    """A deliberately wrong token walk with one planted mistake, from
+    ``planted_walk.c`` (negative controls of the pin tests only)."""
+    return _run("gdn_planted_token_serial", q, k, v, g, beta, h0,
+                cu_seqlens, scale, gate_mode, (int(planted),), lib=_load_planted())
 
 
 def chunked(q, k, v, g, beta, h0, cu_seqlens, scale, gate_mode=GATE_SCALAR,

@@ -79,22 +79,13 @@ void gdn_oracle_set_num_threads(int n) {
 }
 
 /*
- * The token walk.  `planted` selects a deliberately wrong variant used only by
- * the negative-control tests, to show that the pins catch plausible mistakes:
- *   0  the correct recurrence
- *   1  delta taken against the undecayed state (decay applied after the write)
- *   2  output read from the state before the rank-1 write
- *   3  sign of the prediction flipped (u = v + S^T k)
- *   4  beta dropped from the write (S += k u^T)
- *   5  decay applied per value column instead of per key row (KDA)
- *   6  output not scaled
+ * The token walk: the recurrence as stated above, one token at a time.
  */
-static int token_serial_impl(const double *q, const double *k, const double *v,
-                             const double *g, const double *beta,
-                             const double *h0, double *o, double *hT,
-                             const int64_t *cu, int n_seqs, int H, int HV,
-                             int dk, int dv, double scale, int gate_mode,
-                             int planted) {
+int gdn_oracle_token_serial(const double *q, const double *k, const double *v,
+                            const double *g, const double *beta,
+                            const double *h0, double *o, double *hT,
+                            const int64_t *cu, int n_seqs, int H, int HV,
+                            int dk, int dv, double scale, int gate_mode) {
   if (check_common(cu, n_seqs, H, HV, dk, dv, gate_mode)) return 1;
   if (!q || !k || !v || !g || !beta || !o) return 1;
   const int group = HV / H;
@@ -132,15 +123,9 @@ static int token_serial_impl(const double *q, const double *k, const double *v,
           const double *gt = g + ((size_t)t * HV + hv) * dk;
           for (int c = 0; c < dk; c++) a[c] = exp(gt[c]);
         }
-        if (planted != 1) {
-          if (planted == 5) {
-            for (int c = 0; c < dk; c++)
-              for (int j = 0; j < dv; j++) S[(size_t)c * dv + j] *= a[j % dk];
-          } else {
-            for (int c = 0; c < dk; c++)
-              for (int j = 0; j < dv; j++) S[(size_t)c * dv + j] *= a[c];
-          }
-        }
+        /* S = diag(a) S */
+        for (int c = 0; c < dk; c++)
+          for (int j = 0; j < dv; j++) S[(size_t)c * dv + j] *= a[c];
         /* u = v - S^T k */
         for (int j = 0; j < dv; j++) acc[j] = 0.0;
         for (int c = 0; c < dk; c++) {
@@ -148,42 +133,22 @@ static int token_serial_impl(const double *q, const double *k, const double *v,
           const double *Sr = S + (size_t)c * dv;
           for (int j = 0; j < dv; j++) acc[j] += Sr[j] * kc;
         }
-        for (int j = 0; j < dv; j++)
-          u[j] = (planted == 3) ? vt[j] + acc[j] : vt[j] - acc[j];
-        if (planted == 2) {
-          /* read before the write */
-          for (int j = 0; j < dv; j++) acc[j] = 0.0;
-          for (int c = 0; c < dk; c++) {
-            const double qc = qt[c];
-            const double *Sr = S + (size_t)c * dv;
-            for (int j = 0; j < dv; j++) acc[j] += Sr[j] * qc;
-          }
-          for (int j = 0; j < dv; j++)
-            o[((size_t)t * HV + hv) * dv + j] = scale * acc[j];
-        }
+        for (int j = 0; j < dv; j++) u[j] = vt[j] - acc[j];
         /* S += beta k u^T */
-        const double bw = (planted == 4) ? 1.0 : bt;
         for (int c = 0; c < dk; c++) {
-          const double f = bw * kt[c];
+          const double f = bt * kt[c];
           double *Sr = S + (size_t)c * dv;
           for (int j = 0; j < dv; j++) Sr[j] += f * u[j];
         }
-        if (planted == 1) {
-          for (int c = 0; c < dk; c++)
-            for (int j = 0; j < dv; j++) S[(size_t)c * dv + j] *= a[c];
+        /* o = scale S^T q */
+        for (int j = 0; j < dv; j++) acc[j] = 0.0;
+        for (int c = 0; c < dk; c++) {
+          const double qc = qt[c];
+          const double *Sr = S + (size_t)c * dv;
+          for (int j = 0; j < dv; j++) acc[j] += Sr[j] * qc;
         }
-        if (planted != 2) {
-          /* o = scale S^T q */
-          for (int j = 0; j < dv; j++) acc[j] = 0.0;
-          for (int c = 0; c < dk; c++) {
-            const double qc = qt[c];
-            const double *Sr = S + (size_t)c * dv;
-            for (int j = 0; j < dv; j++) acc[j] += Sr[j] * qc;
-          }
-          const double sc = (planted == 6) ? 1.0 : scale;
-          for (int j = 0; j < dv; j++)
-            o[((size_t)t * HV + hv) * dv + j] = sc * acc[j];
-        }
+        for (int j = 0; j < dv; j++)
+          o[((size_t)t * HV + hv) * dv + j] = scale * acc[j];
       }
       if (hT) {
         memcpy(hT + ((size_t)n * HV + hv) * dk * dv, S,
@@ -193,29 +158,6 @@ static int token_serial_impl(const double *q, const double *k, const double *v,
     }
   }
   return failed;
-}
-
-int gdn_oracle_token_serial(const double *q, const double *k, const double *v,
-                            const double *g, const double *beta,
-                            const double *h0, double *o, double *hT,
-                            const int64_t *cu_seqlens, int n_seqs, int H,
-                            int HV, int dk, int dv, double scale,
-                            int gate_mode) {
-  return token_serial_impl(q, k, v, g, beta, h0, o, hT, cu_seqlens, n_seqs, H,
-                           HV, dk, dv, scale, gate_mode, 0);
-}
-
-/* Negative-control entry: the same walk with one planted mistake (see above). */
-int gdn_oracle_token_serial_planted(const double *q, const double *k,
-                                    const double *v, const double *g,
-                                    const double *beta, const double *h0,
-                                    double *o, double *hT,
-                                    const int64_t *cu_seqlens, int n_seqs,
-                                    int H, int HV, int dk, int dv,
-                                    double scale, int gate_mode, int planted) {
-  if (planted < 1 || planted > 6) return 1;
-  return token_serial_impl(q, k, v, g, beta, h0, o, hT, cu_seqlens, n_seqs, H,
-                           HV, dk, dv, scale, gate_mode, planted);
 }
 
 /*

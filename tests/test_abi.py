@@ -33,6 +33,20 @@ def test_header_declares_the_binding_names():
     assert declared_symbols() == sorted(gdn.EXPORTED)
 
 
+def test_status_flag_values_match_the_header():
+    """Each GDN_FLAG_* bit of include/gdn.h has the same value in the binding."""
+    with open(os.path.join(ROOT, "include", "gdn.h")) as f:
+        src = f.read()
+    declared = {name: 1 << int(bit) for name, bit in
+                re.findall(r"\b(GDN_FLAG_\w+)\s*=\s*1u\s*<<\s*(\d+)", src)}
+    assert set(declared) == {"GDN_FLAG_POSITIVE_GATE", "GDN_FLAG_NONFINITE",
+                             "GDN_FLAG_BAD_SEQLENS", "GDN_FLAG_TIMEOUT",
+                             "GDN_FLAG_LAUNCH_CONFIG"}
+    for name, value in declared.items():
+        assert getattr(gdn, name) == value, name
+    assert len(set(declared.values())) == len(declared)
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_symbols():
         assert hasattr(lib, name), name

@@ -7,9 +7,17 @@ B_MMA2, B_MMA3 x2 (tensor-pipe commits).  mbarriers keep phase/parity
 semantics, so a waiter that falls two phases behind blocks as it would on the
 GPU; the tensor pipe runs the issued products in order; every buffer (the
 MMA1 / MMA2 / MMA3 accumulators, the state image, the two Y buffers) carries
-a version stamp, and every read asserts the version it must see.  Random
-delays shake the interleavings.  Negative controls: the model must catch a
-product issued without its wait, and an accumulator ring one buffer short."""
+a version stamp, and every read asserts the version it must see.  The prep
+images arrive in a three-slot ring (the image of chunk c + 1 is copied in once
+MMA1(c) is done).  Random delays shake the interleavings.
+
+Negative controls: the model must catch a product issued without its wait,
+the MMA1 accumulator ring one buffer short, the MMA3 accumulator ring one
+buffer short, and the prep-image ring one slot short.  In each, the warp or
+product that would lose the race is held until the pipe has run the product
+that races it (an event, not a sleep), so the bad interleaving is forced
+whatever the load on the machine; in the protocol as built that product cannot
+run first, and the hold ends on a short timeout."""
 from __future__ import annotations
 
 import queue
@@ -43,12 +51,36 @@ class _MBar:
                 raise RuntimeError(f"{who}: stuck on {self.name} (parity {parity})")
 
 
-def _simulate(nch, *, n_d1=3, n_d3=2, wait_state_before_mma3=True, seed=0,
-              query_delay=0.0, state_delay=0.0):
+def _simulate(nch, *, n_d1=3, n_d3=2, n_p=3, wait_state_before_mma3=True, seed=0,
+              query_delay=0.0, state_delay=0.0, hold=None, hold_timeout=0.05):
+    """``hold``: (who, chunk) -- that party waits, before its racing access at
+    that chunk, for the pipe to have run the product that races it:
+    "state" (S_c's image write vs MMA3(c + 1)), "query_d1" (the read of O_{c-2}
+    from D1 vs MMA1(c + 1)), "query_d3" (the same read from D3 vs MMA3(c)),
+    "mma2" (MMA2(c)'s read of the prep image vs the copy of image c + 1)."""
     rnd = random.Random(seed)
     lock = threading.Lock()
     buf = {}
     errors = []
+    done = {}  # events: products run by the pipe, images copied in
+
+    def event(key):
+        with lock:
+            if key not in done:
+                done[key] = threading.Event()
+            return done[key]
+
+    def release_all():
+        with lock:
+            evs = list(done.values())
+        for ev in evs:
+            ev.set()
+
+    def held(who, c, key):
+        # in the protocol as built the racing product cannot run first, and
+        # the wait ends on its timeout
+        if hold == (who, c):
+            event(key).wait(timeout=hold_timeout)
 
     def jitter():
         if rnd.random() < 0.3:
@@ -87,20 +119,29 @@ def _simulate(nch, *, n_d1=3, n_d3=2, wait_state_before_mma3=True, seed=0,
                 except Exception as e:  # noqa: BLE001
                     errors.append(e)
                     ok = False
+                    release_all()
 
     def commit(name):
         pipe.put(lambda: bars[name].arrive())
 
+    def copy_image(j):  # the prep image of chunk j into slot j % n_p
+        write(("P", j % n_p), ("P", j))
+        event(("P", j)).set()
+
     def mma1(c):  # [E_c; AqkT_{c-1}] Y_{c-1}
         def op():
             read(("Y", (c - 1) & 1), ("Y", c - 1), f"MMA1({c})")
+            read(("P", (c - 1) % n_p), ("P", c - 1), f"MMA1({c})")
             write(("D1", d1(c)), ("MMA1", c))
+            event(("MMA1", c)).set()
         pipe.put(op)
         commit(f"MMA1_{d1(c)}")
 
     def mma2(c):  # P1_{c-1} Y_{c-1}: the state update
         def op():
+            held("mma2", c, ("P", c + 1))
             read(("Y", (c - 1) & 1), ("Y", c - 1), f"MMA2({c})")
+            read(("P", (c - 1) % n_p), ("P", c - 1), f"MMA2({c})")
             write("D2", ("MMA2", c))
         pipe.put(op)
         commit("MMA2")
@@ -109,11 +150,15 @@ def _simulate(nch, *, n_d1=3, n_d3=2, wait_state_before_mma3=True, seed=0,
         def op():
             read("S", ("S", max(e - 1, 0)), f"MMA3({e})")
             write(("D3", d3(e)), ("MMA3", e))
+            event(("MMA3", e)).set()
         pipe.put(op)
         commit(f"MMA3_{d3(e)}")
 
     def issuer():
         try:
+            copy_image(0)
+            if nch > 1:
+                copy_image(1)
             bars["SREADY"].wait(0, "issuer: S_0")
             mma3(0)
             for c in range(1, nch + 1):
@@ -124,6 +169,12 @@ def _simulate(nch, *, n_d1=3, n_d3=2, wait_state_before_mma3=True, seed=0,
                     bars["SREADY"].wait((c - 1) & 1, f"issuer: S_{c - 1}")
                 mma3(c)
                 mma2(c)
+                # the image of chunk c + 1 into the slot of chunk c - 2 once
+                # MMA1(c) is done (the pipe runs in order: MMA2(c - 1), that
+                # slot's last reader, is done too)
+                if c + 1 < nch:
+                    bars[f"MMA1_{d1(c)}"].wait(d1_parity(c), f"issuer: MMA1({c})")
+                    copy_image(c + 1)
         except Exception as e:  # noqa: BLE001
             errors.append(e)
         finally:
@@ -140,7 +191,9 @@ def _simulate(nch, *, n_d1=3, n_d3=2, wait_state_before_mma3=True, seed=0,
                 jitter()
                 if query and c >= 2:  # deferred output of chunk c - 2
                     time.sleep(query_delay)
+                    held("query_d3", c, ("MMA3", c))
                     read(("D3", d3(c - 1)), ("MMA3", c - 1), f"warp {w}: O_{c - 2}")
+                    held("query_d1", c, ("MMA1", c + 1))
                     read(("D1", d1(c - 1)), ("MMA1", c - 1), f"warp {w}: O_{c - 2}")
                 if c >= 1:
                     bars[f"MMA1_{d1(c)}"].wait(d1_parity(c), f"warp {w}: MMA1({c})")
@@ -159,6 +212,7 @@ def _simulate(nch, *, n_d1=3, n_d3=2, wait_state_before_mma3=True, seed=0,
                     if c < nch:
                         if w == 0:
                             time.sleep(state_delay)
+                            held("state", c, ("MMA3", c + 1))
                             write("S", ("S", c))
                         bars["SREADY"].arrive()
             if query:
@@ -195,18 +249,38 @@ def test_protocol_as_built_tolerates_late_warps(slow):
     assert not errors, errors[0]
 
 
-def _caught(delay_key, **mutation):
-    # the late warp's delay only has to outlast the other threads' progress;
-    # longer ones are tried in case the machine is busy
-    return any(_simulate(6, **{delay_key: d}, **mutation) for d in (2e-3, 1e-2, 5e-2))
+@pytest.mark.parametrize("hold", ["state", "query_d1", "query_d3", "mma2"])
+def test_protocol_as_built_survives_every_forced_hold(hold):
+    """The holds of the negative controls, on the protocol as built: each
+    racing product cannot run first, so every hold only ends on its timeout."""
+    for c in (2, 3):
+        errors = _simulate(6, hold=(hold, c))
+        assert not errors, f"hold {hold} at chunk {c}: {errors[0]}"
+
+
+def _caught(hold, **mutation):
+    # the held party waits for the racing product (an event), so the race
+    # happens whatever the machine's load; chunks 2 and 3 are both tried
+    return all(_simulate(6, hold=(hold, c), hold_timeout=2.0, **mutation) for c in (2, 3))
 
 
 def test_model_catches_a_product_issued_without_its_wait():
-    # the state image is written late: MMA3 must wait for it
-    assert _caught("state_delay", wait_state_before_mma3=False)
+    # MMA3(c + 1) sent without waiting for S_c's image
+    assert _caught("state", wait_state_before_mma3=False)
 
 
-def test_model_catches_an_accumulator_ring_one_buffer_short():
+def test_model_catches_an_mma1_accumulator_ring_one_buffer_short():
     # the query lanes read MMA1's accumulator one chunk late, which is why the
-    # kernel keeps three of them: with two, a late reader sees the next product
-    assert _caught("query_delay", n_d1=2)
+    # kernel keeps three of them: with two, MMA1(c + 1) overwrites it first
+    assert _caught("query_d1", n_d1=2)
+
+
+def test_model_catches_an_mma3_accumulator_ring_one_buffer_short():
+    # with one MMA3 accumulator, MMA3(c) overwrites what O_{c-2} still reads
+    assert _caught("query_d3", n_d3=1)
+
+
+def test_model_catches_a_prep_image_ring_one_slot_short():
+    # with two slots, the image of chunk c + 1 lands in the slot MMA2(c)
+    # still reads (waiting for MMA1(c) does not cover MMA2(c))
+    assert _caught("mma2", n_p=2)

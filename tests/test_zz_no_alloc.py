@@ -2,9 +2,11 @@
 device memory (a component whose host framework owns all device memory, or a
 latency-critical loop that must not stall on an allocation).  It takes its
 workspace from a fixed 64 MiB device array inside the library instead of from
-the caller.  These tests call it through the C ABI and check it against
-gdn_chunk_fwd on the same inputs, for two calls in a row (the second call
-reuses the array the first one left behind)."""
+the caller.  These tests call it through the C ABI on the same inputs as
+gdn_chunk_fwd, for two calls in a row (the second call reuses the array the
+first one left behind).  Both routes run the same kernels on the same inputs,
+so their results must agree bit for bit; one case is also checked against the
+fp64 oracle."""
 from __future__ import annotations
 
 import ctypes
@@ -14,7 +16,7 @@ import torch
 
 from chunkwise_gated_delta_gdn_gb300 import build as cuda_build
 from chunkwise_gated_delta_gdn_gb300 import gdn, synth
-from tests.gpu_util import to_dev
+from tests.gpu_util import gpu_heads, kind_of, run_oracle, to_dev
 from tests.metrics import assert_close
 
 
@@ -36,21 +38,45 @@ def call_noalloc(lib, c, d):
     return status, o, hT
 
 
+CASES = [
+    # bf16 scalar gate (GDN), grouped heads
+    synth.case("gdn_bf16_t4096", T=1000, H=4, HV=12),
+    # bf16 per-key gate (KDA)
+    synth.case("kda_bf16_b2_t8192", T=300, H=4, HV=8),
+    # packed sequences with cu_seqlens: the workspace size follows n_seqs
+    synth.case("gdn_varlen_t131072", T=900, H=2, HV=6, n_seqs=5),
+    # fp32 inputs: the other tile layout
+    synth.case("gdn_fp32_t256"),
+]
+
+
 @pytest.mark.gpu
-def test_noalloc_matches_gdn_chunk_fwd_twice_in_a_row():
+@pytest.mark.parametrize("c", CASES, ids=lambda c: c.name)
+def test_noalloc_equals_gdn_chunk_fwd_twice_in_a_row(c):
     lib = gdn.load(cuda_build.build())
-    cases = [synth.case("gdn_bf16_t4096", T=1000, H=4, HV=12),
-             synth.case("kda_bf16_b2_t8192", T=300, H=4, HV=8)]
-    for c in cases:
-        d = to_dev(synth.make_inputs(c))
+    d = to_dev(synth.make_inputs(c))
+    o_ref, h_ref = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
+                                     scale=c.scale, chunk=c.chunk, cu_seqlens=d["cu_seqlens"])
+    for _ in range(2):
         status, o, hT = call_noalloc(lib, c, d)
         assert status == gdn.GDN_OK, gdn.gdn_status_string(status)
-        o_ref, h_ref = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
-                                         scale=c.scale, chunk=c.chunk,
-                                         cu_seqlens=d["cu_seqlens"])
         torch.cuda.synchronize()
-        assert_close(o.cpu(), o_ref.double().cpu(), "bf16", f"{c.name} o")
-        assert_close(hT.cpu(), h_ref.double().cpu(), "bf16", f"{c.name} hT")
+        assert torch.equal(o, o_ref), f"{c.name}: o differs from gdn_chunk_fwd"
+        assert torch.equal(hT, h_ref), f"{c.name}: hT differs from gdn_chunk_fwd"
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_the_oracle():
+    lib = gdn.load(cuda_build.build())
+    c = CASES[0]
+    x = synth.make_inputs(c)
+    status, o, hT = call_noalloc(lib, c, to_dev(x))
+    assert status == gdn.GDN_OK, gdn.gdn_status_string(status)
+    torch.cuda.synchronize()
+    o_ref, h_ref = run_oracle(c, x)
+    og, hg = gpu_heads(o, hT)
+    assert_close(og, o_ref, kind_of(c), f"{c.name} o")
+    assert_close(hg, h_ref, kind_of(c), f"{c.name} hT")
 
 
 def test_noalloc_refuses_requests_beyond_its_array():
