@@ -82,6 +82,41 @@ def algorithmic_bytes(c, which="path"):
     return qk + vo + gb + bb  # scan and whole path: everything once
 
 
+# what each kernel of the split design reads and writes at least once, per
+# chunk slot: the scalar-gate bf16 path's prep writes one 32 KB operand image
+# per value head and one 32 KB [K_next; Q] image per q/k head, which the scan
+# reads back
+KERNEL_BYTES_NOTE = {
+    ("scan", "bf16", 0): "v, o, g, beta plus the prep's operand images read back "
+                         "(HV x 32 KB and H x 32 KB per chunk)",
+    ("prep", "bf16", 0): "q, k, g, beta plus the operand images written "
+                         "(HV x 32 KB and H x 32 KB per chunk)",
+}
+
+
+def kernel_design_bytes(c, which, case, cu_seqlens=None):
+    """Bytes one kernel of the scalar-gate bf16 split design must move; None
+    for the other paths.  ``cu_seqlens``: the packed cuts of a varlen workload."""
+    if (which, c.dtype_name, c.gate_mode) not in KERNEL_BYTES_NOTE:
+        return None
+    n = c.tokens
+    slots = n // c.chunk + case.num_states  # chunk slots the workspace holds (upper bound)
+    chunks = sum(-(-L // c.chunk) for L in seq_lengths(case, cu_seqlens))
+    images = chunks * (c.HV * 32768 + c.H * (c.dk // 64) * 16384)
+    assert chunks <= slots
+    if which == "scan":
+        return 2 * n * c.HV * c.dv * 2 + 2 * n * c.HV * 4 + images
+    return 2 * n * c.H * c.dk * 2 + 2 * n * c.HV * 4 + images
+
+
+def seq_lengths(case, cu_seqlens=None):
+    """Lengths of the sequences of a workload."""
+    if case.n_seqs > 0:
+        cu = [int(v) for v in cu_seqlens]
+        return [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    return [case.T] * case.B
+
+
 def algorithmic_flops(c):
     """Chunk-GEMM FLOPs, dense count: per token and value head
     2 (3 C dk + 2 C dv + 3 dk dv): Gram, W, Aqk; U, O_intra; W S, Qg S, Kt^T Vn."""
@@ -340,6 +375,19 @@ def main():
     prep_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     scan_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
 
+    # (1b) single calls: whole gdn_chunk_fwd passes one after another on one
+    # stream, each finishing before the next starts (what a prefill layer that
+    # must complete before the next layer gets)
+    ev_a = torch.cuda.Event(enable_timing=True)
+    ev_b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev_a.record()
+    for _ in range(K):
+        gdn.gdn_chunk_fwd(*args_in, **kw)
+    ev_b.record()
+    torch.cuda.synchronize()
+    single_ms = max_over_ranks(ev_a.elapsed_time(ev_b) / K, dev)
+
     # (2) throughput pass (the reported value): independent batches in flight
     # on their own streams, each with its own workspace and outputs, so one
     # batch's prep fills the SMs another's scan leaves idle.  Every step is
@@ -469,14 +517,29 @@ def main():
                 "peak_source": f"hbm_gbs of {peak_src}"}
     if traffic_note:
         roofline["traffic_note"] = traffic_note
+    roofline["frac_note"] = ("achieved charges the whole path's algorithmic bytes (q, k, v, o, "
+                             "g, beta read or written once) to this one kernel's launch time")
+    own = kernel_design_bytes(wl, dominant, c0, x["cu_seqlens"])
+    if own is not None:
+        roofline["kernel_own"] = {
+            "bytes": own, "achieved": own / (kern_ms / 1e3) / 1e9,
+            "frac": own / (kern_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "note": "bytes this kernel must move in the split design: " + KERNEL_BYTES_NOTE[
+                (dominant, wl.dtype_name, c0.gate_mode)]}
     path_bytes = algorithmic_bytes(wl, "path")
     path_flops = algorithmic_flops(wl)
     t_hbm = path_bytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = path_flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_tc_burst = path_flops / (peaks["bf16_tflops"] * 1e12)
     path = {"bytes": path_bytes, "flops": path_flops, "t_hbm_us": t_hbm * 1e6,
-            "t_tensor_us": t_tc * 1e6, "bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "t_tensor_us": t_tc * 1e6, "t_tensor_burst_us": t_tc_burst * 1e6,
+            "bound": "hbm" if t_hbm >= t_tc else "tensor",
             "frac": max(t_hbm, t_tc) / (ms_step / 1e3 / world) if ms_step > 0 else None,
-            "note": f"whole path vs max(HBM, tensor) roofline of {peak_src} peaks"}
+            "frac_burst": max(t_hbm, t_tc_burst) / (ms_step / 1e3 / world) if ms_step > 0 else None,
+            "frac_single_call": max(t_hbm, t_tc) / (single_ms / 1e3) if single_ms > 0 else None,
+            "note": f"whole path vs max(HBM, tensor) roofline of {peak_src} peaks; frac uses the "
+                    "sustained bf16 peak (a kernel timed inside a long loop), frac_burst the "
+                    "burst peak"}
 
     # ---- CPU baseline (oracle) on rank 0 at N = 1 ----
     cpu = None
@@ -497,6 +560,10 @@ def main():
                                      "and outputs each); every step is one whole forward pass",
                            kernels_ms="from a separate pass, one step after another"),
             "roofline": roofline, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
+            "single_call": {"value": whole_job_rate(tokens_per_rank, single_ms, world),
+                            "unit": UNIT, "ms_per_step": single_ms,
+                            "note": "one gdn_chunk_fwd after another on one stream, no batches "
+                                    "in flight"},
             "clocks": clocks, "gpu_launches": 2 * K,
             "kernels_ms": {"prep": prep_ms, "scan": scan_ms}, "device_flags": flags}
     if rank == 0:

@@ -233,6 +233,40 @@ __device__ __forceinline__ void warp_mma_tf32x3(float (&acc)[4], float (&corr)[4
   mma1688_tf32(corr, ah, bl0, bl1);
 }
 
+// ---------------------------------------------------------------------------
+// one-pass fp16 warp MMA (m16n8k16): operands rounded once to fp16 (11
+// significand bits), products accumulated in fp32 on the tensor cores.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_f16(float lo_elem, float hi_elem) {
+  const __half2 h = __floats2half2_rn(lo_elem, hi_elem);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void mma16816_f16(float (&c)[4], const uint32_t (&a)[4],
+                                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// acc (a 16 x 8 fp32 tile, accumulator layout) += A B over k = k0 .. k0 + 15;
+// a_at(m, k) and b_at(k, n) give fp32 elements relative to the tile origin.
+template <typename FA, typename FB>
+__device__ __forceinline__ void warp_mma_f16(float (&acc)[4], int k0, FA a_at, FB b_at) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+  const int k = k0 + 2 * tq;
+  uint32_t a[4];
+  a[0] = pack_f16(a_at(gq, k), a_at(gq, k + 1));
+  a[1] = pack_f16(a_at(gq + 8, k), a_at(gq + 8, k + 1));
+  a[2] = pack_f16(a_at(gq, k + 8), a_at(gq, k + 9));
+  a[3] = pack_f16(a_at(gq + 8, k + 8), a_at(gq + 8, k + 9));
+  const uint32_t b0 = pack_f16(b_at(k, gq), b_at(k + 1, gq));
+  const uint32_t b1 = pack_f16(b_at(k + 8, gq), b_at(k + 9, gq));
+  mma16816_f16(acc, a, b0, b1);
+}
+
 // Row / column of accumulator element e of n-tile nt for this lane.
 __device__ __forceinline__ int acc_row(int e) { return ((threadIdx.x & 31) >> 2) + ((e & 2) ? 8 : 0); }
 __device__ __forceinline__ int acc_col(int nt, int e) { return nt * 8 + 2 * (threadIdx.x & 3) + (e & 1); }

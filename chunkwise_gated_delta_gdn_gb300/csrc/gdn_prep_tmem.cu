@@ -18,7 +18,8 @@
 //   T    = (I + A)^-1 blocked as in ROCm/rocm-libraries PR #11223 ("Levers"
 //          3): each 16 x 16 diagonal block by fp32 forward substitution in
 //          registers (one lane per column), then the 32 x 32 and 64 x 64 levels
-//          T10 = -T11 (A10 T00) as split-tf32 mma.sync products (fp32-class)
+//          T10 = -T11 (A10 T00) as one-pass fp16 mma.sync products with fp32
+//          accumulation (T itself enters the later products as fp16 anyway)
 //   P1   = K^T (D T)         the key tile read MN-major, D = diag(exp(b_last - b_s))
 //   AqkT = Aqk T
 //   E    = K_next P1         (fp16 P1 as the B operand; zero for the last chunk
@@ -387,32 +388,24 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       }
       named_bar(1, 128);
       // (2) 32 x 32 blocks from their 16 x 16 halves: T10 = -T11 (A10 T00),
-      //     one warp per (32-block, 8-column tile); split-tf32 tensor-core
-      //     products (fp32-class accuracy), W staged in the warp's rows of Rs
+      //     one warp per (32-block, 8-column tile); one-pass fp16 tensor-core
+      //     products with fp32 accumulation, W staged in the warp's rows of Rs
       const int gq = lane >> 2, tq = lane & 3;
       const bool act2 = wq < 2 * (C / 32);
       const int ob = 32 * (wq >> 1), n2 = 8 * (wq & 1);
       float *Wt2 = Rs + wq * 16 * 9;  // this warp's 16 x 8 W tile, row stride 9
       if (act2) {
-        float w[4] = {0.f, 0.f, 0.f, 0.f}, wc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k0 = 0; k0 < 16; k0 += 8)
-          warp_mma_tf32x3(w, wc, k0, [&](int m, int k) { return As[(ob + k) * LDT + ob + 16 + m]; },
-                          [&](int k, int n) { return As[(ob + n2 + n) * LDT + ob + k]; });
-#pragma unroll
-        for (int e = 0; e < 4; e++) w[e] += wc[e];
+        float w[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_mma_f16(w, 0, [&](int m, int k) { return As[(ob + k) * LDT + ob + 16 + m]; },
+                     [&](int k, int n) { return As[(ob + n2 + n) * LDT + ob + k]; });
         Wt2[gq * 9 + 2 * tq] = w[0]; Wt2[gq * 9 + 2 * tq + 1] = w[1];
         Wt2[(gq + 8) * 9 + 2 * tq] = w[2]; Wt2[(gq + 8) * 9 + 2 * tq + 1] = w[3];
       }
       named_bar(1, 128);  // both warps of a block have read A10 before T10 overwrites it
       if (act2) {
-        float u[4] = {0.f, 0.f, 0.f, 0.f}, uc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k0 = 0; k0 < 16; k0 += 8)
-          warp_mma_tf32x3(u, uc, k0, [&](int m, int k) { return As[(ob + 16 + k) * LDT + ob + 16 + m]; },
-                          [&](int k, int n) { return Wt2[k * 9 + n]; });
-#pragma unroll
-        for (int e = 0; e < 4; e++) u[e] += uc[e];
+        float u[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_mma_f16(u, 0, [&](int m, int k) { return As[(ob + 16 + k) * LDT + ob + 16 + m]; },
+                     [&](int k, int n) { return Wt2[k * 9 + n]; });
         // T10[r][c] -> As[(ob + n2 + c) LDT + ob + 16 + r], over A10^T
         As[(ob + n2 + 2 * tq) * LDT + ob + 16 + gq] = -u[0];
         As[(ob + n2 + 2 * tq + 1) * LDT + ob + 16 + gq] = -u[1];
@@ -424,17 +417,13 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
         // (3) the 64 x 64 inverse from its 32 x 32 halves: T10 = -T11 (A10 T00),
         //     warp w owns columns 8w .. 8w+7 of W and of T10
         const int n0 = 8 * wq;
-        float w[2][4] = {}, wc[2][4] = {};
+        float w[2][4] = {};
 #pragma unroll
-        for (int k0 = 0; k0 < 32; k0 += 8)
+        for (int k0 = 0; k0 < 32; k0 += 16)
 #pragma unroll
           for (int mt = 0; mt < 2; mt++)
-            warp_mma_tf32x3(w[mt], wc[mt], k0, [&](int m, int k) { return As[k * LDT + 32 + 16 * mt + m]; },
-                            [&](int k, int n) { return As[(n0 + n) * LDT + k]; });
-#pragma unroll
-        for (int mt = 0; mt < 2; mt++)
-#pragma unroll
-          for (int e = 0; e < 4; e++) w[mt][e] += wc[mt][e];
+            warp_mma_f16(w[mt], k0, [&](int m, int k) { return As[k * LDT + 32 + 16 * mt + m]; },
+                         [&](int k, int n) { return As[(n0 + n) * LDT + k]; });
         float *Wt = Rs + wq * 32 * 9;  // this warp's 32 x 8 W tile, row stride 9
 #pragma unroll
         for (int mt = 0; mt < 2; mt++) {
@@ -442,18 +431,14 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
           Wt[(16 * mt + gq + 8) * 9 + 2 * tq] = w[mt][2]; Wt[(16 * mt + gq + 8) * 9 + 2 * tq + 1] = w[mt][3];
         }
         named_bar(1, 128);  // every warp has read A10 before T10 overwrites it
-        float u[2][4] = {}, uc[2][4] = {};
+        float u[2][4] = {};
 #pragma unroll
-        for (int k0 = 0; k0 < 32; k0 += 8)
+        for (int k0 = 0; k0 < 32; k0 += 16)
 #pragma unroll
           for (int mt = 0; mt < 2; mt++)
             if (k0 < 16 * (mt + 1))  // T11 lower triangular
-              warp_mma_tf32x3(u[mt], uc[mt], k0, [&](int m, int k) { return As[(32 + k) * LDT + 32 + 16 * mt + m]; },
-                              [&](int k, int n) { return Wt[k * 9 + n]; });
-#pragma unroll
-        for (int mt = 0; mt < 2; mt++)
-#pragma unroll
-          for (int e = 0; e < 4; e++) u[mt][e] += uc[mt][e];
+              warp_mma_f16(u[mt], k0, [&](int m, int k) { return As[(32 + k) * LDT + 32 + 16 * mt + m]; },
+                           [&](int k, int n) { return Wt[k * 9 + n]; });
 #pragma unroll
         for (int mt = 0; mt < 2; mt++) {
           As[(n0 + 2 * tq) * LDT + 32 + 16 * mt + gq] = -u[mt][0];

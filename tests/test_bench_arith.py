@@ -79,3 +79,26 @@ def test_whole_job_rate_and_metric_names():
     assert bench.metric_of(synth.case("gdn_decode_bf16_b256")) == bench.METRIC_DECODE
     assert bench.metric_of(synth.case("prepost_bf16_t32768")) == bench.METRIC_PREPOST
     assert bench.metric_of(synth.case("gdn_bf16_t32768")) == bench.METRIC
+
+
+def test_kernel_own_bytes_of_the_split_design():
+    """The scan of the 32k workload reads v (48*128*2 B/token), g and beta
+    (2*48*4) and writes o (48*128*2), and reads back the prep's images: per
+    chunk 48 value-head images of 32 KB and 16 [K_next; Q] images of 32 KB,
+    512 chunks.  The prep reads q, k (2*16*128*2), g and beta and writes those
+    images.  (ncu measured 1.87 and 1.33 GB of DRAM traffic for the two
+    kernels.)"""
+    c0, w = view("gdn_bf16_t32768")
+    images = 512 * (48 + 16) * 32768
+    assert images == 1_073_741_824
+    assert bench.kernel_design_bytes(w, "scan", c0) == 32768 * (2 * 12288 + 384) + images
+    assert bench.kernel_design_bytes(w, "prep", c0) == 32768 * (8192 + 384) + images
+    # packed: chunks are counted per sequence (a ragged tail is a whole chunk)
+    cv, wv = view("gdn_varlen_t131072")
+    cu = [0, 100, 164, 131072 - 1, 131072, 131072, 131072, 131072, 131072]
+    chunks = 2 + 1 + (131072 - 1 - 164 + 63) // 64 + 1
+    assert bench.kernel_design_bytes(wv, "scan", cv, cu) == (
+        131072 * (2 * 12288 + 384) + chunks * 64 * 32768)
+    # other paths have no split-design figure
+    ck, wk = view("kda_bf16_b2_t8192")
+    assert bench.kernel_design_bytes(wk, "scan", ck) is None
