@@ -59,6 +59,8 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-lockstep", action="store_true",
+                    help="skip the lockstep launch's timing pass")
     ap.add_argument("--in-flight", type=int, default=3,
                     help="independent batches in flight in the throughput pass (3 measured "
                          "best at 32k tokens: 2 / 3 / 4 give 34.0 / 35.5 / 34.6 M tokens/s)")
@@ -388,6 +390,20 @@ def main():
     torch.cuda.synchronize()
     single_ms = max_over_ranks(ev_a.elapsed_time(ev_b) / K, dev)
 
+    # (1c) the lockstep launch (prep and scan in one cooperative grid), where
+    # the path has one: single calls one after another, as (1b)
+    lock_ms = None
+    if wl.dtype_name == "bf16" and c0.gate_mode == 0 and not args.no_lockstep:
+        for _ in range(2):
+            gdn.gdn_chunk_fwd_lockstep(*args_in, **kw)
+        torch.cuda.synchronize()
+        ev_a.record()
+        for _ in range(K):
+            gdn.gdn_chunk_fwd_lockstep(*args_in, **kw)
+        ev_b.record()
+        torch.cuda.synchronize()
+        lock_ms = max_over_ranks(ev_a.elapsed_time(ev_b) / K, dev)
+
     # (2) throughput pass (the reported value): independent batches in flight
     # on their own streams, each with its own workspace and outputs, so one
     # batch's prep fills the SMs another's scan leaves idle.  Every step is
@@ -560,6 +576,11 @@ def main():
                                      "and outputs each); every step is one whole forward pass",
                            kernels_ms="from a separate pass, one step after another"),
             "roofline": roofline, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
+            "lockstep": None if lock_ms is None else {
+                "value": whole_job_rate(tokens_per_rank, lock_ms, world), "unit": UNIT,
+                "ms_per_step": lock_ms,
+                "note": "gdn_chunk_fwd_lockstep (prep and scan in one cooperative launch), one "
+                        "call after another; an ablation against the split kernels"},
             "single_call": {"value": whole_job_rate(tokens_per_rank, single_ms, world),
                             "unit": UNIT, "ms_per_step": single_ms,
                             "note": "one gdn_chunk_fwd after another on one stream, no batches "

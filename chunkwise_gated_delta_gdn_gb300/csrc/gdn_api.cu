@@ -76,6 +76,7 @@ struct Plan {
   size_t tile_bytes;
   size_t kq_bytes;
   size_t decay_bytes;
+  size_t ready_bytes;
   size_t ws_bytes;
 };
 
@@ -118,7 +119,12 @@ gdn_status plan(int B, int T, int H, int HV, int dk, int dv, int chunk,
     p.kq_bytes = (size_t)p.n_slots * heads * (size_t)gdn::kq_image_bytes(dk);
     if (gate_mode == GDN_GATE_PER_KEY) p.decay_bytes = (size_t)p.n_slots * HV * dk * sizeof(float);
   }
-  p.ws_bytes = gdn::kWorkspaceHeader + p.tile_bytes + p.kq_bytes + p.decay_bytes;
+  // bf16 scalar gate: one ready flag per (slot, q/k head) for the lockstep
+  // launch, 256-byte padded
+  p.ready_bytes = 0;
+  if (dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR)
+    p.ready_bytes = ((size_t)p.n_slots * (size_t)H * sizeof(int) + 255) / 256 * 256;
+  p.ws_bytes = gdn::kWorkspaceHeader + p.tile_bytes + p.kq_bytes + p.decay_bytes + p.ready_bytes;
   return GDN_OK;
 }
 
@@ -153,7 +159,7 @@ size_t gdn_chunk_fwd_workspace_bytes(int B, int T, int H, int HV, int dk, int dv
 
 namespace {
 
-enum Stage { kPrep = 1, kScan = 2, kBoth = 3 };
+enum Stage { kPrep = 1, kScan = 2, kBoth = 3, kLockstep = 4 };
 
 gdn_status run(int stages, const void *q, const void *k, const void *v, const float *g,
                const float *beta, const float *h0, void *o, float *hT,
@@ -166,6 +172,9 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
   gdn_status st = plan(B, T, H, HV, dk, dv, chunk, gate_mode, n_seqs, dtype, packed, p);
   if (st != GDN_OK) return st;
   if (!std::isfinite(scale)) return GDN_ERR_INVALID_ARG;
+  // the lockstep launch exists for the bf16 scalar-gate path only
+  if (stages == kLockstep && !(dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR))
+    return GDN_ERR_UNSUPPORTED;
 
   // pointers: required ones non-null (token data may be absent when there are
   // no tokens), all 16-byte aligned
@@ -209,11 +218,37 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
                                                             gdn::kWorkspaceHeader + p.tile_bytes +
                                                             p.kq_bytes)
                                 : nullptr;
+  int *ready = p.ready_bytes ? reinterpret_cast<int *>(static_cast<char *>(workspace) +
+                                                       gdn::kWorkspaceHeader + p.tile_bytes +
+                                                       p.kq_bytes + p.decay_bytes)
+                             : nullptr;
 
   gdn::ScanMaps maps;
   if (dtype == GDN_BF16 &&
       !gdn::make_scan_maps(maps, q, k, v, (int)p.Ttot, H, HV, dk, dv, chunk))
     return GDN_ERR_CUDA;
+  if (stages == kLockstep) {
+    if (cudaMemsetAsync(flags, 0, sizeof(uint32_t), stream) != cudaSuccess) return GDN_ERR_CUDA;
+    if (p.Ttot == 0 && !hT) return GDN_OK;
+    if (cudaMemsetAsync(ready, 0, p.ready_bytes, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    gdn::PrepArgs pa;
+    pa.q = q; pa.k = k; pa.g = g; pa.beta = beta;
+    pa.seq = seq; pa.H = H; pa.HV = HV; pa.scale = scale;
+    pa.tiles = tiles; pa.flags = flags; pa.n_slots = (int)p.n_slots;
+    pa.kq_images = kq_images;
+    pa.decays = decays;
+    gdn::ScanArgs sa;
+    sa.q = q; sa.k = k; sa.v = v; sa.g = g; sa.beta = beta; sa.h0 = h0;
+    sa.o = o; sa.hT = hT; sa.seq = seq; sa.H = H; sa.HV = HV; sa.dv = dv;
+    sa.scale = scale; sa.tiles = tiles; sa.flags = flags; sa.kq_images = kq_images;
+    sa.decays = decays;
+    const cudaError_t e = gdn::launch_lockstep(pa, sa, maps, ready, chunk, dk, stream);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+      (void)cudaGetLastError();
+      return GDN_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  }
   if (stages & kPrep) {
     if (cudaMemsetAsync(flags, 0, sizeof(uint32_t), stream) != cudaSuccess) return GDN_ERR_CUDA;
     if (p.Ttot > 0) {
@@ -262,6 +297,16 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
                          int dtype, void *workspace, size_t workspace_bytes,
                          gdn_stream_t stream) {
   return run(kBoth, q, k, v, g, beta, h0, o, hT, cu_seqlens, n_seqs, B, T, H, HV, dk, dv,
+             chunk, scale, gate_mode, dtype, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_chunk_fwd_lockstep(const void *q, const void *k, const void *v, const float *g,
+                                  const float *beta, const float *h0, void *o, float *hT,
+                                  const int32_t *cu_seqlens, int n_seqs, int B, int T, int H,
+                                  int HV, int dk, int dv, int chunk, float scale, int gate_mode,
+                                  int dtype, void *workspace, size_t workspace_bytes,
+                                  gdn_stream_t stream) {
+  return run(kLockstep, q, k, v, g, beta, h0, o, hT, cu_seqlens, n_seqs, B, T, H, HV, dk, dv,
              chunk, scale, gate_mode, dtype, workspace, workspace_bytes, stream);
 }
 

@@ -142,6 +142,12 @@ cudaError_t launch_prep_tmem(const PrepArgs &a, const ScanMaps &maps, int chunk,
                              cudaStream_t stream);
 cudaError_t launch_scan_la(const ScanArgs &a, const ScanMaps &maps, int chunk, int dk,
                            cudaStream_t stream);
+// the same two computations in one cooperative launch, the scan loading each
+// prep image once the prep has set its (chunk slot, q/k head) flag in
+// `ready` (n_slots x H ints, zeroed beforehand); cudaErrorCooperativeLaunchTooLarge
+// when the scan's blocks leave no SM for the prep
+cudaError_t launch_lockstep(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &maps,
+                            int *ready, int chunk, int dk, cudaStream_t stream);
 // causal depthwise convolution (width 1..4, D a multiple of 8; activation 0 =
 // none, 1 = SiLU) and the row norms (kind 0 = L2, 1 = gated RMS; dim 64, 128
 // or 256)

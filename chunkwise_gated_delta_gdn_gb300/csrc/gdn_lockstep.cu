@@ -1,0 +1,116 @@
+// gdn_lockstep.cu -- the chunk prep and the scan of the bf16 scalar-gate (GDN)
+// path in one launch, in lockstep (the fused prep + scan composition of
+// ROCm/rocm-libraries PR #11223, "Summary", in a form for this GPU).
+//
+// The grid is cooperative, so that every CTA is resident at once.  Its first
+// n_scan CTAs are the scan's blocks (gdn_scan_la.cuh, unchanged arithmetic);
+// the others run the prep (gdn_prep_tmem.cuh, unchanged arithmetic) in three
+// persistent warpgroups each, over the (chunk slot, q/k head) units in chunk
+// order.  A warpgroup that finishes a unit waits for its bulk stores to
+// complete and sets that unit's ready flag (release, gpu scope); the scan loads
+// a prep image only once its flag is set (acquire, bounded wait).  The prep
+// never waits for the scan, so the scan always makes progress, and the images
+// of a chunk are read back soon after they are written.
+//
+// Both halves run the same device code as the split kernels, on the same
+// inputs, so the results equal gdn_chunk_fwd's bit for bit.  The prep has only
+// the SMs the scan leaves (one CTA per SM: the scan needs about 213 KB of
+// shared memory), three warpgroups each: fewer units in flight than the split
+// prep kernel's three CTAs on every SM.
+#include "gdn_prep_tmem.cuh"
+#include "gdn_scan_la.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace sm100;
+
+constexpr int kPrepGroups = 3;  // prep warpgroups per prep CTA
+
+template <int C, int DK>
+struct LockSmem {
+  static constexpr int kScan = LaSmem<C, DK>::kUsed;
+  static constexpr int kPrep = kPrepGroups * PrepTmemSmem<C>::kSlice;
+  static constexpr int kUsed = kScan > kPrep ? kScan : kPrep;
+  static constexpr int kBytes = kUsed + 1024;  // alignment slack
+  static_assert(kThreads >= kPrepGroups * 128, "prep warpgroups of one CTA");
+  static_assert(kBytes <= 232448, "shared memory of one CTA");
+};
+
+template <int C, int DK>
+__global__ void __launch_bounds__(kThreads, 1)
+gdn_lockstep_kernel(const PrepArgs pa, const ScanArgs sa, const __grid_constant__ ScanMaps maps,
+                    int n_scan, int *ready) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
+  if (blockIdx.x < (unsigned)n_scan) {
+    scan_la_block<C, DK>(sa, maps, blockIdx.x, sm, ready);
+    return;
+  }
+  // ---- prep CTA: three warpgroups, each its own slice and 128 columns ----
+  using PS = PrepTmemSmem<C>;
+  const int wg = threadIdx.x >> 7;
+  // the address slot: the first word at kMisc of warpgroup 0's slice, which
+  // the unit leaves to its caller
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + PS::kMisc);
+  constexpr uint32_t kCols = 512;
+  unsigned char *wsm = sm + wg * PS::kSlice;
+  if (threadIdx.x < 32) tmem_alloc(smem_addr(tslot), kCols);
+  if ((threadIdx.x & 127) == 0 && wg < kPrepGroups) prep_tmem_init_barriers<C>(wsm);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tslot;
+  if (wg < kPrepGroups) {
+    const int groups = (gridDim.x - n_scan) * kPrepGroups;
+    const int units = pa.n_slots * pa.H;
+    PrepPhases ph;  // the slice's barriers stay initialised across units
+    for (int u = (blockIdx.x - n_scan) * kPrepGroups + wg; u < units; u += groups)
+      prep_tmem_unit<C, DK>(pa, maps, u / pa.H, u % pa.H, wsm, tmem + 128u * wg,
+                            threadIdx.x & 127, 1 + wg, ready, ph);
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (threadIdx.x < 32) tmem_dealloc(tmem, kCols);
+}
+
+template <int C, int DK>
+cudaError_t launch_one(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &maps,
+                       int *ready, cudaStream_t stream) {
+  using SM = LockSmem<C, DK>;
+  auto kern = gdn_lockstep_kernel<C, DK>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+  if (err != cudaSuccess) return err;
+  int dev = 0, n_sm = 0, per_sm = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return err;
+  if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, SM::kBytes)) !=
+      cudaSuccess)
+    return err;
+  const long n_scan = (long)sa.seq.n_seqs * sa.HV * (sa.dv / kScanTcSlice);
+  const long resident = (long)n_sm * per_sm;
+  if (per_sm < 1 || n_scan + 1 > resident) return cudaErrorCooperativeLaunchTooLarge;
+  int n_scan_i = (int)n_scan;
+  PrepArgs pa_ = pa;
+  ScanArgs sa_ = sa;
+  ScanMaps maps_ = maps;
+  void *args[] = {&pa_, &sa_, &maps_, &n_scan_i, &ready};
+  return cudaLaunchCooperativeKernel((const void *)kern, dim3((unsigned)resident), dim3(kThreads),
+                                     args, SM::kBytes, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_lockstep(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &maps,
+                            int *ready, int chunk, int dk, cudaStream_t stream) {
+  if (chunk == 64 && dk == 128) return launch_one<64, 128>(pa, sa, maps, ready, stream);
+  if (chunk == 64 && dk == 64) return launch_one<64, 64>(pa, sa, maps, ready, stream);
+  if (chunk == 32 && dk == 128) return launch_one<32, 128>(pa, sa, maps, ready, stream);
+  if (chunk == 32 && dk == 64) return launch_one<32, 64>(pa, sa, maps, ready, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gdn

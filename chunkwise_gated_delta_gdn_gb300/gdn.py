@@ -41,6 +41,7 @@ GDN_FLAG_LAUNCH_CONFIG = 1 << 4
 # every symbol include/gdn.h declares
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_chunk_fwd_workspace_bytes",
             "gdn_chunk_fwd", "gdn_chunk_fwd_prep", "gdn_chunk_fwd_scan",
+            "gdn_chunk_fwd_lockstep",
             "gdn_chunk_fwd_noalloc", "gdn_recurrent_fwd", "gdn_causal_conv1d_fwd",
             "gdn_l2norm_fwd", "gdn_rmsnorm_gated_fwd", "gdn_state_combine",
             "gdn_selftest_wait", "gdn_read_device_flags")
@@ -78,7 +79,8 @@ def load(path: Optional[str] = None):
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_chunk_fwd_workspace_bytes.argtypes = [i32] * 10
         lib.gdn_chunk_fwd_workspace_bytes.restype = sz
-        for name in ("gdn_chunk_fwd", "gdn_chunk_fwd_prep", "gdn_chunk_fwd_scan"):
+        for name in ("gdn_chunk_fwd", "gdn_chunk_fwd_prep", "gdn_chunk_fwd_scan",
+                     "gdn_chunk_fwd_lockstep"):
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                            i32, i32, i32, i32, i32, f32, i32, i32, vp, sz, vp]
@@ -201,6 +203,21 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     """
     return _call("gdn_chunk_fwd", q, k, v, g, beta, h0, scale, chunk, cu_seqlens, o, hT,
                  output_final_state, workspace, stream)
+
+
+def gdn_chunk_fwd_lockstep(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                           beta: torch.Tensor, h0: Optional[torch.Tensor] = None, *,
+                           scale: Optional[float] = None, chunk: int = 64,
+                           cu_seqlens: Optional[torch.Tensor] = None,
+                           o: Optional[torch.Tensor] = None, hT: Optional[torch.Tensor] = None,
+                           output_final_state: bool = True,
+                           workspace: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None
+                           ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """gdn_chunk_fwd with prep and scan in one cooperative launch, in lockstep
+    (bf16 inputs, scalar gate only); same arguments and results."""
+    return _call("gdn_chunk_fwd_lockstep", q, k, v, g, beta, h0, scale, chunk, cu_seqlens, o,
+                 hT, output_final_state, workspace, stream)
 
 
 def gdn_chunk_fwd_prep(q, k, v, g, beta, h0=None, *, workspace: torch.Tensor,

@@ -166,6 +166,30 @@ GDN_API gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
  * arguments and workspace; gdn_chunk_fwd_prep followed by gdn_chunk_fwd_scan
  * computes exactly what gdn_chunk_fwd computes.
  */
+/*
+ * gdn_chunk_fwd with its two kernels in one launch, in lockstep: the fused
+ * prep + scan composition of ROCm/rocm-libraries PR #11223 ("Summary"), built
+ * for this GPU as a cooperative grid.  Its first CTAs run the scan's blocks;
+ * the rest run the chunk prep in persistent warpgroups, chunk by chunk, and
+ * set a ready flag per (chunk, q/k head) in the workspace once that unit's
+ * operand images are complete; the scan loads an image only after its flag
+ * (bounded wait: GDN_FLAG_TIMEOUT if a flag never comes).  Same arguments,
+ * checks, workspace and results as gdn_chunk_fwd, bit for bit: both run the
+ * same per-chunk and per-block device code.  Only the bf16 scalar-gate (GDN)
+ * path has it: other dtype / gate combinations return GDN_ERR_UNSUPPORTED,
+ * as does a problem whose scan blocks (sequences x HV x dv/64) leave no SM
+ * for the prep.  The split kernels are faster here (the prep gets only the
+ * SMs the scan leaves); this entry exists to measure the fused composition
+ * against them (PR #11223, "Notes for reviewers").
+ */
+GDN_API gdn_status gdn_chunk_fwd_lockstep(const void *q, const void *k, const void *v,
+                              const float *g, const float *beta, const float *h0,
+                              void *o, float *hT, const int32_t *cu_seqlens,
+                              int n_seqs, int B, int T, int H, int HV, int dk,
+                              int dv, int chunk, float scale, int gate_mode,
+                              int dtype, void *workspace, size_t workspace_bytes,
+                              gdn_stream_t stream);
+
 GDN_API gdn_status gdn_chunk_fwd_prep(const void *q, const void *k, const void *v,
                               const float *g, const float *beta, const float *h0,
                               void *o, float *hT, const int32_t *cu_seqlens,

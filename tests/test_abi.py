@@ -61,9 +61,12 @@ def test_status_strings(lib):
 
 def test_workspace_query(lib):
     # bf16, scalar gate: header + (T/C + N) slots x (HV x one 32 KB fp16 operand
-    # image [P1; E; AqkT] + H x one 32 KB fp16 [K_next; Q] image)
+    # image [P1; E; AqkT] + H x one 32 KB fp16 [K_next; Q] image), then one int ready flag per
+    # (slot, q/k head) for the lockstep launch, padded to 256 bytes
+    slots = 32768 // 64 + 1
     ws = gdn.gdn_chunk_fwd_workspace_bytes(1, 32768, 16, 48, 128, 128, 64, 0, 1, gdn.GDN_BF16)
-    assert ws == 256 + (32768 // 64 + 1) * (48 * 256 * 128 + 16 * 2 * 128 * 128)
+    assert ws == (256 + slots * (48 * 256 * 128 + 16 * 2 * 128 * 128)
+                  + (slots * 16 * 4 + 255) // 256 * 256)
     # bf16, per-key gate: per (slot, value head) one 24 KB image [P1; AqkT], one
     # 32 KB gated [K~; Q~] image and dk fp32 chunk decays
     ws = gdn.gdn_chunk_fwd_workspace_bytes(2, 8192, 32, 32, 128, 128, 32, 1, 2, gdn.GDN_BF16)
@@ -123,6 +126,25 @@ def call(lib, **kw):
 ])
 def test_refusals(lib, kw, status):
     assert call(lib, **kw) == status
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(dtype=0), gdn.GDN_ERR_UNSUPPORTED),       # fp32: no lockstep launch
+    (dict(gate_mode=1, chunk=32), gdn.GDN_ERR_UNSUPPORTED),   # per-key gate
+    (dict(q=None), gdn.GDN_ERR_INVALID_ARG),        # the same checks as gdn_chunk_fwd
+    (dict(ws_bytes=1000), gdn.GDN_ERR_WORKSPACE),
+    (dict(hT=addr(5)), gdn.GDN_ERR_INVALID_ARG),
+])
+def test_lockstep_refusals(lib, kw, status):
+    a = dict(q=addr(0), k=addr(1), v=addr(2), g=addr(3), beta=addr(4), h0=addr(5),
+             o=addr(6), hT=addr(7), cu=None, n_seqs=1, B=1, T=128, H=2, HV=4, dk=128,
+             dv=128, chunk=64, scale=0.088, gate_mode=0, dtype=1, ws=addr(8),
+             ws_bytes=1 << 30)
+    a.update(kw)
+    assert lib.gdn_chunk_fwd_lockstep(
+        a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["o"], a["hT"], a["cu"],
+        a["n_seqs"], a["B"], a["T"], a["H"], a["HV"], a["dk"], a["dv"], a["chunk"],
+        a["scale"], a["gate_mode"], a["dtype"], a["ws"], a["ws_bytes"], None) == status
 
 
 def test_read_flags_rejects_null(lib):
