@@ -55,13 +55,35 @@ struct PrepTcSmem {
   static constexpr int kG = kR + 16 * LDC * 4;                 // gates -> b -> Kt
   static constexpr int kBeta = kG + C * LDG * 4;
   static constexpr int kMeta = kBeta + C * 4;
-  // factored operands of one 16-row block (K~, Q~, then K^ for
-  // up to C rows), fp32, row stride LDX
-  static constexpr int LDX = DK + 4;
-  static constexpr int kX = (kMeta + 16 + 15) / 16 * 16;
-  static constexpr int kBytes = kX + (32 + C) * LDX * 4;
+  // factored operands of one 16-row block, each split into bf16 hi and lo
+  // planes (x = hi + lo, 16 significant bits, the fp32 exponent range):
+  // K~ hi, K~ lo, Q~ hi, Q~ lo (16 rows each), then K^ hi, K^ lo (C rows
+  // each); bf16 row stride LDH (a 16-byte multiple, rows 272 bytes apart so
+  // that ldmatrix's eight row reads fall in different banks)
+  static constexpr int LDH = DK + 8;
+  static constexpr int kX = (kMeta + 16 + 127) / 128 * 128;
+  static constexpr int kBytes = kX + (4 * 16 + 2 * C) * LDH * 2;
   static_assert(kImgSpan >= kPrepImageBytes, "image must fit the Q + A regions");
 };
+
+// four 8 x 8 bf16 matrices (x4) / two (x2) from rows of shared memory: lane l
+// gives the address of one row (mma.sync fragment order)
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t &r0, uint32_t &r1, uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(saddr));
+}
+
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi), four values at a time
+__device__ __forceinline__ void split4(float4 x, uint2 &hi, uint2 &lo) {
+  split2(x.x, x.y, hi.x, lo.x);
+  split2(x.z, x.w, hi.y, lo.y);
+}
 
 __device__ __forceinline__ void put_f16(unsigned char *img, int row, int col, float v) {
   *reinterpret_cast<__half *>(img + sm100::kmajor_off(row, col, kPrepImageRows)) = __float2half_rn(v);
@@ -163,13 +185,15 @@ gdn_prep_tc_kernel(const PrepArgs a) {
     //   Aqk[r][s] = scale  sum_c (q_rc e^{b_rc - b_oc}) (k_sc e^{b_oc - b_sc})
     // r in the block, s <= o + 15: the row factors are <= 1, the column factors
     // <= 1 for s <= o and at most e^{-(sum of the block's gates)} inside it.
-    // Products on the tensor cores in split tf32 (fp32-class accuracy).  When
-    // an in-block factor could leave the fp32 range the CTA falls back to
-    // forming every pairwise decay directly.
-    float *Xk = reinterpret_cast<float *>(smem + SM::kX);
-    float *Xq = Xk + 16 * SM::LDX;
-    float *Kh = Xq + 16 * SM::LDX;
-    constexpr int LDX = SM::LDX;
+    // Products on the tensor cores in split bf16: each factored operand is
+    // written once as hi + lo bf16 planes (16 significant bits, the fp32
+    // exponent range the factors need) and read back by ldmatrix.  When an
+    // in-block factor could leave the fp32 range the CTA falls back to forming
+    // every pairwise decay directly.
+    constexpr int LDH = SM::LDH;
+    __nv_bfloat16 *Xkh = reinterpret_cast<__nv_bfloat16 *>(smem + SM::kX);
+    __nv_bfloat16 *Xkl = Xkh + 16 * LDH, *Xqh = Xkl + 16 * LDH, *Xql = Xqh + 16 * LDH;
+    __nv_bfloat16 *Khh = Xql + 16 * LDH, *Khl = Khh + C * LDH;
     bool wide = false;
     for (int idx = tid; idx < C * DK; idx += kThreads) {
       const int s = idx / DK, c = idx % DK, o = s & ~15;
@@ -192,30 +216,51 @@ gdn_prep_tc_kernel(const PrepArgs a) {
           const float4 bo = *reinterpret_cast<const float4 *>(Gs + o * LDG + c);
           const float4 e = make_float4(__expf(b.x - bo.x), __expf(b.y - bo.y), __expf(b.z - bo.z), __expf(b.w - bo.w));
           const float4 kv = bf4(Kb + (o + r) * LDB + c), qv = bf4(Qb + (o + r) * LDB + c);
-          *reinterpret_cast<float4 *>(Xk + r * LDX + c) = make_float4(kv.x * e.x, kv.y * e.y, kv.z * e.z, kv.w * e.w);
-          *reinterpret_cast<float4 *>(Xq + r * LDX + c) = make_float4(qv.x * e.x, qv.y * e.y, qv.z * e.z, qv.w * e.w);
+          uint2 h, l;
+          split4(make_float4(kv.x * e.x, kv.y * e.y, kv.z * e.z, kv.w * e.w), h, l);
+          *reinterpret_cast<uint2 *>(Xkh + r * LDH + c) = h;
+          *reinterpret_cast<uint2 *>(Xkl + r * LDH + c) = l;
+          split4(make_float4(qv.x * e.x, qv.y * e.y, qv.z * e.z, qv.w * e.w), h, l);
+          *reinterpret_cast<uint2 *>(Xqh + r * LDH + c) = h;
+          *reinterpret_cast<uint2 *>(Xql + r * LDH + c) = l;
         }
         for (int idx = tid; idx < ns * DK / 4; idx += kThreads) {
           const int r = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
           const float4 b = *reinterpret_cast<const float4 *>(Gs + r * LDG + c);
           const float4 bo = *reinterpret_cast<const float4 *>(Gs + o * LDG + c);
           const float4 kv = bf4(Kb + r * LDB + c);
-          *reinterpret_cast<float4 *>(Kh + r * LDX + c) =
-              make_float4(kv.x * __expf(bo.x - b.x), kv.y * __expf(bo.y - b.y), kv.z * __expf(bo.z - b.z),
-                          kv.w * __expf(bo.w - b.w));
+          uint2 h, l;
+          split4(make_float4(kv.x * __expf(bo.x - b.x), kv.y * __expf(bo.y - b.y),
+                             kv.z * __expf(bo.z - b.z), kv.w * __expf(bo.w - b.w)), h, l);
+          *reinterpret_cast<uint2 *>(Khh + r * LDH + c) = h;
+          *reinterpret_cast<uint2 *>(Khl + r * LDH + c) = l;
         }
         __syncthreads();
-        // tiles of 8 columns: ns / 8 for A, as many for Aqk
+        // tiles of 8 columns: ns / 8 for A, as many for Aqk.  Per 16-deep step
+        // the fragments come by ldmatrix from the hi / lo planes and three
+        // bf16 products (hi hi, lo hi, hi lo) accumulate in fp32.
         const int ntile = ns / 8;
+        const uint32_t a_row = (lane & 15) * LDH + (lane >> 4) * 8;       // A fragment row
+        const uint32_t b_row = (lane & 7) * LDH + ((lane >> 3) & 1) * 8;  // B fragment row
         for (int tile = warp; tile < 2 * ntile; tile += kThreads / 32) {
           const bool isq = tile >= ntile;
           const int n0 = 8 * (isq ? tile - ntile : tile);
-          const float *X = isq ? Xq : Xk;
+          const uint32_t sAh = sm100::smem_addr(isq ? Xqh : Xkh) + 2 * a_row;
+          const uint32_t sAl = sm100::smem_addr(isq ? Xql : Xkl) + 2 * a_row;
+          const uint32_t sBh = sm100::smem_addr(Khh + n0 * LDH) + 2 * b_row;
+          const uint32_t sBl = sm100::smem_addr(Khl + n0 * LDH) + 2 * b_row;
           float acc[4] = {0.f, 0.f, 0.f, 0.f}, corr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-          for (int k0 = 0; k0 < DK; k0 += 8)
-            warp_mma_tf32x3(acc, corr, k0, [&](int m, int k) { return X[m * LDX + k]; },
-                            [&](int k, int n) { return Kh[(n0 + n) * LDX + k]; });
+          for (int k0 = 0; k0 < DK; k0 += 16) {
+            uint32_t ah[4], al[4], bh0, bh1, bl0, bl1;
+            ldsm_x4(ah, sAh + 2 * k0);
+            ldsm_x4(al, sAl + 2 * k0);
+            ldsm_x2(bh0, bh1, sBh + 2 * k0);
+            ldsm_x2(bl0, bl1, sBl + 2 * k0);
+            mma16816(acc, ah, bh0, bh1);
+            mma16816(corr, al, bh0, bh1);
+            mma16816(corr, ah, bl0, bl1);
+          }
 #pragma unroll
           for (int e = 0; e < 4; e++) {
             const int r = o + acc_row(e), sc = n0 + acc_col(0, e);
