@@ -579,8 +579,8 @@ def main():
             "lockstep": None if lock_ms is None else {
                 "value": whole_job_rate(tokens_per_rank, lock_ms, world), "unit": UNIT,
                 "ms_per_step": lock_ms,
-                "note": "gdn_chunk_fwd_lockstep (prep and scan in one cooperative launch), one "
-                        "call after another; an ablation against the split kernels"},
+                "note": "gdn_chunk_fwd_lockstep (the prep's first half of the chunks, then prep "
+                        "and scan in one cooperative launch), one call after another"},
             "single_call": {"value": whole_job_rate(tokens_per_rank, single_ms, world),
                             "unit": UNIT, "ms_per_step": single_ms,
                             "note": "one gdn_chunk_fwd after another on one stream, no batches "

@@ -138,16 +138,21 @@ cudaError_t launch_scan_tc(const ScanArgs &a, const ScanMaps &maps, int chunk, i
                            int gate, cudaStream_t stream);
 // bf16 scalar-gate path: prep on tensor memory writing the lookahead image,
 // and the lookahead scan consuming it
+// (n_slots >= 0: only the first n_slots chunk slots; ready != nullptr: each
+// unit's flag in ready[slot * H + hq] is set once its images are complete)
 cudaError_t launch_prep_tmem(const PrepArgs &a, const ScanMaps &maps, int chunk, int dk,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int n_slots = -1, int *ready = nullptr);
 cudaError_t launch_scan_la(const ScanArgs &a, const ScanMaps &maps, int chunk, int dk,
                            cudaStream_t stream);
 // the same two computations in one cooperative launch, the scan loading each
 // prep image once the prep has set its (chunk slot, q/k head) flag in
-// `ready` (n_slots x H ints, zeroed beforehand); cudaErrorCooperativeLaunchTooLarge
-// when the scan's blocks leave no SM for the prep
+// `ready` (n_slots x H ints, zeroed beforehand); the prep warpgroups take the
+// units from slot `head_slots` on (the earlier ones come from a prep launch
+// over the first head_slots slots, enqueued just before);
+// cudaErrorCooperativeLaunchTooLarge when the scan's blocks leave no SM for
+// the prep
 cudaError_t launch_lockstep(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &maps,
-                            int *ready, int chunk, int dk, cudaStream_t stream);
+                            int *ready, int head_slots, int chunk, int dk, cudaStream_t stream);
 // causal depthwise convolution (width 1..4, D a multiple of 8; activation 0 =
 // none, 1 = SiLU) and the row norms (kind 0 = L2, 1 = gated RMS; dim 64, 128
 // or 256)

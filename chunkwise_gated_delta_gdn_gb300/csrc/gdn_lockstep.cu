@@ -16,7 +16,10 @@
 // inputs, so the results equal gdn_chunk_fwd's bit for bit.  The prep has only
 // the SMs the scan leaves (one CTA per SM: the scan needs about 213 KB of
 // shared memory), three warpgroups each: fewer units in flight than the split
-// prep kernel's three CTAs on every SM.
+// prep kernel's three CTAs on every SM.  So the prep gets a head start: the
+// split prep kernel runs first over the first head_slots chunk slots on every
+// SM, setting their flags as well, and the lockstep's prep warpgroups take the
+// slots after them while the scan walks the chunks.
 #include "gdn_prep_tmem.cuh"
 #include "gdn_scan_la.cuh"
 
@@ -40,7 +43,7 @@ struct LockSmem {
 template <int C, int DK>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_lockstep_kernel(const PrepArgs pa, const ScanArgs sa, const __grid_constant__ ScanMaps maps,
-                    int n_scan, int *ready) {
+                    int n_scan, int *ready, int unit0) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
   if (blockIdx.x < (unsigned)n_scan) {
@@ -65,7 +68,7 @@ gdn_lockstep_kernel(const PrepArgs pa, const ScanArgs sa, const __grid_constant_
     const int groups = (gridDim.x - n_scan) * kPrepGroups;
     const int units = pa.n_slots * pa.H;
     PrepPhases ph;  // the slice's barriers stay initialised across units
-    for (int u = (blockIdx.x - n_scan) * kPrepGroups + wg; u < units; u += groups)
+    for (int u = unit0 + (blockIdx.x - n_scan) * kPrepGroups + wg; u < units; u += groups)
       prep_tmem_unit<C, DK>(pa, maps, u / pa.H, u % pa.H, wsm, tmem + 128u * wg,
                             threadIdx.x & 127, 1 + wg, ready, ph);
   }
@@ -77,7 +80,7 @@ gdn_lockstep_kernel(const PrepArgs pa, const ScanArgs sa, const __grid_constant_
 
 template <int C, int DK>
 cudaError_t launch_one(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &maps,
-                       int *ready, cudaStream_t stream) {
+                       int *ready, int head_slots, cudaStream_t stream) {
   using SM = LockSmem<C, DK>;
   auto kern = gdn_lockstep_kernel<C, DK>;
   cudaError_t err =
@@ -93,11 +96,17 @@ cudaError_t launch_one(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &m
   const long n_scan = (long)sa.seq.n_seqs * sa.HV * (sa.dv / kScanTcSlice);
   const long resident = (long)n_sm * per_sm;
   if (per_sm < 1 || n_scan + 1 > resident) return cudaErrorCooperativeLaunchTooLarge;
+  // the head start: the split prep kernel over the first head_slots slots
+  head_slots = head_slots < 0 ? 0 : (head_slots > pa.n_slots ? pa.n_slots : head_slots);
+  if (head_slots > 0 &&
+      (err = launch_prep_tmem(pa, maps, C, DK, stream, head_slots, ready)) != cudaSuccess)
+    return err;
   int n_scan_i = (int)n_scan;
+  int unit0 = head_slots * pa.H;
   PrepArgs pa_ = pa;
   ScanArgs sa_ = sa;
   ScanMaps maps_ = maps;
-  void *args[] = {&pa_, &sa_, &maps_, &n_scan_i, &ready};
+  void *args[] = {&pa_, &sa_, &maps_, &n_scan_i, &ready, &unit0};
   return cudaLaunchCooperativeKernel((const void *)kern, dim3((unsigned)resident), dim3(kThreads),
                                      args, SM::kBytes, stream);
 }
@@ -105,11 +114,11 @@ cudaError_t launch_one(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &m
 }  // namespace
 
 cudaError_t launch_lockstep(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &maps,
-                            int *ready, int chunk, int dk, cudaStream_t stream) {
-  if (chunk == 64 && dk == 128) return launch_one<64, 128>(pa, sa, maps, ready, stream);
-  if (chunk == 64 && dk == 64) return launch_one<64, 64>(pa, sa, maps, ready, stream);
-  if (chunk == 32 && dk == 128) return launch_one<32, 128>(pa, sa, maps, ready, stream);
-  if (chunk == 32 && dk == 64) return launch_one<32, 64>(pa, sa, maps, ready, stream);
+                            int *ready, int head_slots, int chunk, int dk, cudaStream_t stream) {
+  if (chunk == 64 && dk == 128) return launch_one<64, 128>(pa, sa, maps, ready, head_slots, stream);
+  if (chunk == 64 && dk == 64) return launch_one<64, 64>(pa, sa, maps, ready, head_slots, stream);
+  if (chunk == 32 && dk == 128) return launch_one<32, 128>(pa, sa, maps, ready, head_slots, stream);
+  if (chunk == 32 && dk == 64) return launch_one<32, 64>(pa, sa, maps, ready, head_slots, stream);
   return cudaErrorInvalidValue;
 }
 

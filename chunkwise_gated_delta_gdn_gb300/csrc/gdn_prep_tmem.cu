@@ -2,7 +2,9 @@
 // path: one CTA of 128 threads per (chunk slot, q/k head), running the unit of
 // gdn_prep_tmem.cuh.  Three CTAs share an SM (128 tensor-memory columns and
 // about 75 KB of shared memory each), so that their latency-bound phases
-// overlap.
+// overlap.  Launched over every slot before the scan kernel, or over the first
+// slots only, publishing each unit's ready flag, ahead of the lockstep launch
+// (gdn_lockstep.cu).
 #include "gdn_prep_tmem.cuh"
 
 namespace gdn {
@@ -12,7 +14,7 @@ using namespace sm100;
 
 template <int C, int DK>
 __global__ void __launch_bounds__(128, 3)
-gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
+gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps, int *ready) {
   extern __shared__ unsigned char smem_raw[];
   // 1 KB-aligned base, as an offset into the shared array (the compiler then
   // knows every access below is to shared memory)
@@ -26,7 +28,7 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   fence_after_sync();
   const uint32_t tmem = *tslot;
   PrepPhases ph;
-  prep_tmem_unit<C, DK>(a, maps, blockIdx.x, blockIdx.y, sm, tmem, threadIdx.x, 1, nullptr, ph);
+  prep_tmem_unit<C, DK>(a, maps, blockIdx.x, blockIdx.y, sm, tmem, threadIdx.x, 1, ready, ph);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -34,7 +36,8 @@ gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
 }
 
 template <int C, int DK>
-cudaError_t launch_one(const PrepArgs &a, const ScanMaps &maps, cudaStream_t stream) {
+cudaError_t launch_one(const PrepArgs &a, const ScanMaps &maps, int n_slots, int *ready,
+                       cudaStream_t stream) {
   using SM = PrepTmemSmem<C>;
   auto kern = gdn_prep_tmem_kernel<C, DK>;
   cudaError_t err =
@@ -43,18 +46,20 @@ cudaError_t launch_one(const PrepArgs &a, const ScanMaps &maps, cudaStream_t str
   // three CTAs per SM need the largest shared-memory carve-out
   err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (err != cudaSuccess) return err;
-  kern<<<dim3(a.n_slots, a.H), 128, SM::kBytes, stream>>>(a, maps);
+  kern<<<dim3(n_slots, a.H), 128, SM::kBytes, stream>>>(a, maps, ready);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prep_tmem(const PrepArgs &a, const ScanMaps &maps, int chunk, int dk,
-                             cudaStream_t stream) {
-  if (chunk == 64 && dk == 128) return launch_one<64, 128>(a, maps, stream);
-  if (chunk == 64 && dk == 64) return launch_one<64, 64>(a, maps, stream);
-  if (chunk == 32 && dk == 128) return launch_one<32, 128>(a, maps, stream);
-  if (chunk == 32 && dk == 64) return launch_one<32, 64>(a, maps, stream);
+                             cudaStream_t stream, int n_slots, int *ready) {
+  if (n_slots < 0) n_slots = a.n_slots;
+  if (n_slots == 0) return cudaSuccess;
+  if (chunk == 64 && dk == 128) return launch_one<64, 128>(a, maps, n_slots, ready, stream);
+  if (chunk == 64 && dk == 64) return launch_one<64, 64>(a, maps, n_slots, ready, stream);
+  if (chunk == 32 && dk == 128) return launch_one<32, 128>(a, maps, n_slots, ready, stream);
+  if (chunk == 32 && dk == 64) return launch_one<32, 64>(a, maps, n_slots, ready, stream);
   return cudaErrorInvalidValue;
 }
 
