@@ -11,7 +11,8 @@
 //            blocks; ROCm/rocm-libraries PR #11223, "Levers" 3)
 //   P1     = Kt^T T       (Kt_s = k_s exp(b_last - b_s); dk x C)
 //   AqkT   = Aqk T        (C x C)
-// and writes P1 and AqkT, rounded once to fp16, as one 24 KB operand image in
+// and writes P1 and AqkT (tcgen05 products of fp16 operands, fp32 accumulation
+// in tensor memory), rounded once to fp16, as one 24 KB operand image in
 // the scan kernel's shared-memory layout (K-major, 128-byte swizzle, 192 rows
 // of 64 elements: rows 0..127 = P1 (rows >= dk zero), rows 128..191 = AqkT,
 // columns >= C zero).  With Y = diag(beta)(V - Kg S) the scan then needs only
@@ -20,9 +21,10 @@
 // #1296 ("What this is") folded into P1 and AqkT so that no dk-wide W ever
 // crosses HBM.  It also publishes the scan's gated operand image [Kg; Qg]
 // (Kg = k e^b, Qg = scale q e^b, fp16) and the chunk's per-channel decay
-// e^{b_last}.  Every product here runs on the tensor cores in split precision
-// (split tf32 or split bf16, fp32 accumulation); the images are the only
-// rounding to fp16.
+// e^{b_last}.  The factored A / Aqk products run on the tensor cores in split
+// bf16 (mma.sync, 16 significant bits and the fp32 range their factors need);
+// P1 and Aqk T, whose operands stay within fp16, run as tcgen05 products like
+// the scalar-gate path's.  The image is stored with one bulk copy.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -61,9 +63,23 @@ struct PrepTcSmem {
   // each); bf16 row stride LDH (a 16-byte multiple, rows 272 bytes apart so
   // that ldmatrix's eight row reads fall in different banks)
   static constexpr int LDH = DK + 8;
-  static constexpr int kX = (kMeta + 16 + 127) / 128 * 128;
-  static constexpr int kBytes = kX + (4 * 16 + 2 * C) * LDH * 2;
+  static constexpr int kBar = (kMeta + 16 + 7) / 8 * 8;      // the products' mbarrier
+  static constexpr int kTslot = kBar + 8;                    // tensor-memory address
+  static constexpr int kAbort = kTslot + 4;
+  static constexpr int kX = (kAbort + 4 + 1023) / 1024 * 1024;
+  static constexpr int XBYTES = (4 * 16 + 2 * C) * LDH * 2;
+  // Once A and Aqk are formed, the X region holds the fp16 operands of the
+  // image products (K-major, 128-byte swizzle): Kt as C token rows x dk in
+  // two 64-channel panels (read MN-major: M = dk), T as C rows (row j =
+  // column j of T), Aqk as 128 rows (rows >= C not written; their products
+  // are not read)
+  static constexpr int kOpKt = kX;
+  static constexpr int kOpT = kOpKt + 2 * C * 128;
+  static constexpr int kOpAqk = kOpT + C * 128;
+  static constexpr int kBytes = kX + (XBYTES > 2 * C * 128 + C * 128 + 128 * 128
+                                          ? XBYTES : 2 * C * 128 + C * 128 + 128 * 128) + 1024;
   static_assert(kImgSpan >= kPrepImageBytes, "image must fit the Q + A regions");
+  static_assert(kX % 1024 == 0 && kOpT % 1024 == 0 && kOpAqk % 1024 == 0, "operand alignment");
 };
 
 // four 8 x 8 bf16 matrices (x4) / two (x2) from rows of shared memory: lane l
@@ -85,15 +101,14 @@ __device__ __forceinline__ void split4(float4 x, uint2 &hi, uint2 &lo) {
   split2(x.z, x.w, hi.y, lo.y);
 }
 
-__device__ __forceinline__ void put_f16(unsigned char *img, int row, int col, float v) {
-  *reinterpret_cast<__half *>(img + sm100::kmajor_off(row, col, kPrepImageRows)) = __float2half_rn(v);
-}
 
 template <int C, int DK>
 __global__ void __launch_bounds__(kThreads)
 gdn_prep_tc_kernel(const PrepArgs a) {
   using SM = PrepTcSmem<C, DK>;
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ unsigned char smem_raw[];
+  // 1 KB-aligned base (the tensor-core operands use the 128-byte swizzle)
+  unsigned char *smem = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
   __nv_bfloat16 *Kb = reinterpret_cast<__nv_bfloat16 *>(smem + SM::kK);
   __nv_bfloat16 *Qb = reinterpret_cast<__nv_bfloat16 *>(smem + SM::kQ);
   float *As = reinterpret_cast<float *>(smem + SM::kA);
@@ -129,6 +144,17 @@ gdn_prep_tc_kernel(const PrepArgs a) {
   __syncthreads();
   if (!meta[2]) return;
   const int t0 = meta[0], L = meta[1];
+  // tensor memory for the image products: P1 at column 0, Aqk T at 64
+  constexpr uint32_t kTmemCols = 128;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + SM::kTslot);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kAbort);
+  const uint32_t bar_mma = sm100::smem_addr(smem + SM::kBar);
+  if (warp == 0) sm100::tmem_alloc(sm100::smem_addr(tslot), kTmemCols);
+  if (tid == 0) {
+    *abort_flag = 0;
+    sm100::mbar_init(bar_mma, 1);
+    sm100::mbar_fence_init();
+  }
 
   // ---- loads ----
   {
@@ -376,51 +402,102 @@ gdn_prep_tc_kernel(const PrepArgs a) {
         Gs[r * LDG + c] = __bfloat162float(Kb[r * LDB + c]) * __expf(bl - Gs[r * LDG + c]);
     }
   }
-  // ---- the image (Q and A are dead now): zero, then P1 and AqkT ----
-  for (int idx = tid; idx < kPrepImageBytes / 16; idx += kThreads)
-    reinterpret_cast<uint4 *>(img)[idx] = make_uint4(0, 0, 0, 0);
-  __syncthreads();
-
-  // AqkT = Aqk T  (3-pass split)
+  __syncthreads();  // Kt complete; every reader of the X planes is done
+  // ---- fp16 operands of the image products, into the dead X region ----
   {
-    constexpr int NMT = C / 16, NNG = C / 32;
-    for (int task = warp; task < NMT * NNG; task += kThreads / 32) {
-      const int m0 = (task / NNG) * 16, n0 = (task % NNG) * 32;
-      float acc[4][4] = {};
-      warp_mma<C, 4, false, false>(
-          acc, [&](int m, int k) { return Aqks[(m0 + m) * LDC + k]; },
-          [&](int k, int n) { return Ts[k * LDC + n0 + n]; });
+    unsigned char *opKt = smem + SM::kOpKt, *opT = smem + SM::kOpT, *opAqk = smem + SM::kOpAqk;
+    // Kt: token row r, channels 8 at a time (two panels, the second zero when dk = 64)
+    for (int idx = tid; idx < C * 16; idx += kThreads) {
+      const int r = idx / 16, c8 = (idx % 16) * 8;
+      uint4 pk = make_uint4(0, 0, 0, 0);
+      if (c8 < DK) {
+        __half2 *h = reinterpret_cast<__half2 *>(&pk);
 #pragma unroll
-      for (int nt = 0; nt < 4; nt++)
-#pragma unroll
-        for (int e = 0; e < 4; e++)
-          put_f16(img, kPrepImageRows - 64 + m0 + acc_row(e), n0 + acc_col(nt, e), acc[nt][e]);
-    }
-  }
-  // P1 = Kt^T T  (Kt split)
-  {
-    constexpr int NMT = DK / 16, NNG = C / 32;
-    for (int task = warp; task < NMT * NNG; task += kThreads / 32) {
-      const int m0 = (task / NNG) * 16, n0 = (task % NNG) * 32;
-      float acc[4][4] = {};
-      {
-        warp_mma<C, 4, false, false>(
-            acc, [&](int m, int k) { return Gs[k * LDG + m0 + m]; },
-            [&](int k, int n) { return Ts[k * LDC + n0 + n]; });
+        for (int i = 0; i < 4; i++) h[i] = __floats2half2_rn(Gs[r * LDG + c8 + 2 * i], Gs[r * LDG + c8 + 2 * i + 1]);
       }
-#pragma unroll
-      for (int nt = 0; nt < 4; nt++)
-#pragma unroll
-        for (int e = 0; e < 4; e++) put_f16(img, m0 + acc_row(e), n0 + acc_col(nt, e), acc[nt][e]);
+      *reinterpret_cast<uint4 *>(opKt + sm100::kmajor_off(r, c8, C)) = pk;
     }
+    // T as the B operand (row j = T[.][j]) and Aqk as the A operand (row r =
+    // Aqk[r][.]), 64 columns per row, zero beyond C
+    for (int idx = tid; idx < 2 * C * 8; idx += kThreads) {
+      const bool isT = idx < C * 8;
+      const int row = (idx % (C * 8)) / 8, k8 = (idx % 8) * 8;
+      uint4 pk = make_uint4(0, 0, 0, 0);
+      if (k8 < C) {
+        __half2 *h = reinterpret_cast<__half2 *>(&pk);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const int k = k8 + 2 * i;
+          h[i] = isT ? __floats2half2_rn(Ts[k * LDC + row], Ts[(k + 1) * LDC + row])
+                     : __floats2half2_rn(Aqks[row * LDC + k], Aqks[row * LDC + k + 1]);
+        }
+      }
+      *reinterpret_cast<uint4 *>((isT ? opT : opAqk) + sm100::kmajor_off(row, k8, isT ? C : 128)) = pk;
+    }
+    // the output image (Q and A are dead now) starts at zero
+    for (int idx = tid; idx < kPrepImageBytes / 16; idx += kThreads)
+      reinterpret_cast<uint4 *>(img)[idx] = make_uint4(0, 0, 0, 0);
+  }
+  sm100::fence_proxy_async();
+  sm100::fence_before_sync();
+  __syncthreads();
+  sm100::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  // ---- P1 = Kt^T T (M = dk rows, N = C, K = C) and Aqk T (rows < C) on
+  //      the tensor cores, fp16 operands, fp32 accumulation ----
+  if (tid == 0) {
+    const uint32_t sKt = sm100::smem_addr(smem + SM::kOpKt), sT = sm100::smem_addr(smem + SM::kOpT);
+    const uint32_t sAqk = sm100::smem_addr(smem + SM::kOpAqk);
+    constexpr uint32_t idP = sm100::idesc_f16(128, C, 1, 0);  // Kt read MN-major
+    constexpr uint32_t idQ = sm100::idesc_f16(128, C, 0, 0);
+#pragma unroll
+    for (int k0 = 0; k0 < C; k0 += 16) {
+      const uint64_t bd = sm100::make_desc(sT + k0 * 2, 16, 1024);
+      sm100::mma_f16(tmem, sm100::make_desc(sKt + k0 * 128, C * 128, 1024), bd, idP, k0 > 0 ? 1u : 0u);
+      sm100::mma_f16(tmem + 64, sm100::make_desc(sAqk + k0 * 2, 16, 1024), bd, idQ, k0 > 0 ? 1u : 0u);
+    }
+    sm100::mma_commit(bar_mma);
+  }
+  sm100::mbar_wait(bar_mma, 0, abort_flag);
+  sm100::fence_after_sync();
+  // ---- read back: lane t holds row t of P1 (t < dk) and of Aqk T (t < C) ----
+  {
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    auto put_row = [&](int row, uint32_t taddr) {
+#pragma unroll
+      for (int h = 0; h < C / 32; h++) {
+        uint32_t v[32];
+        sm100::tmem_ld32_nowait(taddr + 32 * h, v);
+        sm100::tmem_wait_ld();
+#pragma unroll
+        for (int ch = 0; ch < 4; ch++) {
+          uint4 pk;
+          __half2 *hh = reinterpret_cast<__half2 *>(&pk);
+#pragma unroll
+          for (int i = 0; i < 4; i++)
+            hh[i] = __floats2half2_rn(__uint_as_float(v[ch * 8 + 2 * i]), __uint_as_float(v[ch * 8 + 2 * i + 1]));
+          *reinterpret_cast<uint4 *>(img + sm100::kmajor_off(row, 32 * h + ch * 8, kPrepImageRows)) = pk;
+        }
+      }
+    };
+    if (tid < DK) put_row(tid, tmem + lane_base);
+    if (tid < C) put_row(kPrepImageRows - 64 + tid, tmem + lane_base + 64);
+  }
+  sm100::fence_proxy_async();
+  sm100::fence_before_sync();
+  __syncthreads();
+  sm100::fence_after_sync();
+
+  // ---- image -> workspace, one bulk copy ----
+  if (tid == 0) {
+    unsigned char *dst = reinterpret_cast<unsigned char *>(a.tiles) + ((size_t)slot * a.HV + hv) * kPrepImageBytes;
+    sm100::bulk_s2g(dst, sm100::smem_addr(img), kPrepImageBytes);
+    sm100::bulk_commit();
+    sm100::bulk_wait_read_all();
+    if (*abort_flag) atomicOr(a.flags, kFlagTimeout);
   }
   __syncthreads();
-
-  // ---- image -> workspace ----
-  uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(a.tiles) +
-                                         ((size_t)slot * a.HV + hv) * kPrepImageBytes);
-  for (int idx = tid; idx < kPrepImageBytes / 16; idx += kThreads)
-    dst[idx] = reinterpret_cast<const uint4 *>(img)[idx];
+  if (warp == 0) sm100::tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int C, int DK>
