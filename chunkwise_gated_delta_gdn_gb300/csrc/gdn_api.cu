@@ -46,15 +46,29 @@ bool map3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t 
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 tensor [d2][d1][d0] (d0 contiguous), box {b0, 1, b2}, no swizzle
+bool map3d_f32(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint32_t b0, uint32_t b2) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
+  const cuuint32_t box[3] = {b0, 1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
-bool make_scan_maps(ScanMaps &m, const void *q, const void *k, const void *v, int Ttot, int H,
-                    int HV, int dk, int dv, int chunk) {
+bool make_scan_maps(ScanMaps &m, const void *q, const void *k, const void *v,
+                    const float *g_per_key, int Ttot, int H, int HV, int dk, int dv, int chunk) {
   std::memset(&m, 0, sizeof(m));
   if (Ttot <= 0) return true;  // nothing will be loaded
   if (!encode_fn()) return false;
   return map3d(&m.q, q, dk, H, Ttot, 64, chunk) && map3d(&m.k, k, dk, H, Ttot, 64, chunk) &&
-         map3d(&m.v, v, dv, HV, Ttot, kScanTcSlice, chunk);
+         map3d(&m.v, v, dv, HV, Ttot, kScanTcSlice, chunk) &&
+         (!g_per_key || map3d_f32(&m.g, g_per_key, dk, HV, Ttot, 64, chunk));
 }
 
 }  // namespace gdn
@@ -231,7 +245,8 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
 
   gdn::ScanMaps maps;
   if (dtype == GDN_BF16 &&
-      !gdn::make_scan_maps(maps, q, k, v, (int)p.Ttot, H, HV, dk, dv, chunk))
+      !gdn::make_scan_maps(maps, q, k, v, gate_mode == GDN_GATE_PER_KEY ? g : nullptr,
+                           (int)p.Ttot, H, HV, dk, dv, chunk))
     return GDN_ERR_CUDA;
   if (stages == kLockstep) {
     if (cudaMemsetAsync(flags, 0, sizeof(uint32_t), stream) != cudaSuccess) return GDN_ERR_CUDA;
@@ -268,6 +283,8 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
       cudaError_t e;
       if (dtype == GDN_BF16 && gate_mode == GDN_GATE_SCALAR)
         e = gdn::launch_prep_tmem(pa, maps, chunk, dk, stream);
+      else if (dtype == GDN_BF16 && chunk == 32)
+        e = gdn::launch_prep_kda(pa, maps, dk, stream);
       else if (dtype == GDN_BF16)
         e = gdn::launch_prep_tc(pa, chunk, dk, gate_mode, stream);
       else

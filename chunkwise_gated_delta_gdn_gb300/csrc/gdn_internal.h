@@ -125,15 +125,20 @@ cudaError_t launch_scan(const ScanArgs &a, int chunk, int dk, int dtype,
 // [Ttot][HV][dv], boxes of 64 columns x 1 head x C tokens, 128-byte swizzle.
 struct ScanMaps {
   CUtensorMap q, k, v;
+  CUtensorMap g;  // per-key gates (fp32 [Ttot][HV][dk], box 64 x 1 x chunk); zero otherwise
 };
-// Encode the three maps (host); false when the driver refuses.
-bool make_scan_maps(ScanMaps &m, const void *q, const void *k, const void *v, int Ttot,
-                    int H, int HV, int dk, int dv, int chunk);
+// Encode the maps (host); `g_per_key` null for the scalar gate.  False when
+// the driver refuses.
+bool make_scan_maps(ScanMaps &m, const void *q, const void *k, const void *v,
+                    const float *g_per_key, int Ttot, int H, int HV, int dk, int dv, int chunk);
 
 // bf16 per-key-gate path: prep writing fp16 operand images, tcgen05 scan
 // consuming them
 cudaError_t launch_prep_tc(const PrepArgs &a, int chunk, int dk, int gate,
                            cudaStream_t stream);
+// bf16 per-key-gate prep at chunk 32 (gdn_prep_kda.cu): TMA tiles, the
+// factored A / Aqk product on tcgen05; same outputs as launch_prep_tc
+cudaError_t launch_prep_kda(const PrepArgs &a, const ScanMaps &maps, int dk, cudaStream_t stream);
 cudaError_t launch_scan_tc(const ScanArgs &a, const ScanMaps &maps, int chunk, int dk,
                            int gate, cudaStream_t stream);
 // bf16 scalar-gate path: prep on tensor memory writing the lookahead image,
