@@ -530,7 +530,10 @@ def main():
         ("prep", "bf16", 1): "gdn_prep_tc_kernel", ("scan", "bf16", 1): "gdn_scan_tc_kernel",
         ("prep", "f32", 0): "gdn_prep_kernel", ("scan", "f32", 0): "gdn_scan_kernel",
         ("prep", "f32", 1): "gdn_prep_kernel", ("scan", "f32", 1): "gdn_scan_kernel"}
-    roofline = {"bound": "hbm", "kernel": kernel_names[(dominant, wl.dtype_name, c0.gate_mode)],
+    kname = kernel_names[(dominant, wl.dtype_name, c0.gate_mode)]
+    if kname == "gdn_prep_tc_kernel" and c0.chunk == 32:
+        kname = "gdn_prep_kda_kernel"  # the per-key-gate prep at chunk 32
+    roofline = {"bound": "hbm", "kernel": kname,
                 "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic, "algorithmic_bytes": kbytes, "kernel_ms": kern_ms,
