@@ -333,14 +333,25 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
         uint32_t g[32];
         tmem_ld32_nowait(tmem + lane_base + 32 * h, g);
         tmem_wait_ld();
+        // the block's 32 column factors (cross-block factors or cumulative
+        // gates), four at a time
+        float fv[32];
+        {
+          const float *src = 32 * h < o ? Wf : Gs + 32 * h;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 f4 = *reinterpret_cast<const float4 *>(src + i);
+            fv[i] = f4.x; fv[i + 1] = f4.y; fv[i + 2] = f4.z; fv[i + 3] = f4.w;
+          }
+        }
         if (32 * h < o) {
 #pragma unroll
-          for (int i = 0; i < 32; i++) As[(32 * h + i) * LDT + r] = bu * __uint_as_float(g[i]) * Wf[i];
+          for (int i = 0; i < 32; i++) As[(32 * h + i) * LDT + r] = bu * __uint_as_float(g[i]) * fv[i];
         } else {
 #pragma unroll
           for (int i = 0; i < 32; i++) {
             const int s = 32 * h + i;
-            As[s * LDT + r] = s < r ? beta * __uint_as_float(g[i]) * ex2(br - Gs[s]) : 0.f;
+            As[s * LDT + r] = s < r ? beta * __uint_as_float(g[i]) * ex2(br - fv[i]) : 0.f;
           }
         }
       }
@@ -357,6 +368,15 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
           tmem_ld32_nowait(tmem + lane_base + 32 * h, g);
           tmem_wait_ld();
         }
+        float fv[32];
+        if (any) {
+          const float *src = 32 * h < o ? Wf : Gs + 32 * h;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 f4 = *reinterpret_cast<const float4 *>(src + i);
+            fv[i] = f4.x; fv[i + 1] = f4.y; fv[i + 2] = f4.z; fv[i + 3] = f4.w;
+          }
+        }
 #pragma unroll
         for (int ch = 0; ch < 4; ch++) {
           uint4 pk;
@@ -364,13 +384,14 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
 #pragma unroll
           for (int i = 0; i < 4; i++) {
             const int s = 32 * h + ch * 8 + 2 * i;
+            const int ii = ch * 8 + 2 * i;
             float v0 = 0.f, v1 = 0.f;
             if (32 * h < o) {
-              v0 = su * __uint_as_float(g[ch * 8 + 2 * i]) * Wf[s];
-              v1 = su * __uint_as_float(g[ch * 8 + 2 * i + 1]) * Wf[s + 1];
+              v0 = su * __uint_as_float(g[ii]) * fv[ii];
+              v1 = su * __uint_as_float(g[ii + 1]) * fv[ii + 1];
             } else if (any) {
-              v0 = s <= r ? a.scale * __uint_as_float(g[ch * 8 + 2 * i]) * ex2(br - Gs[s]) : 0.f;
-              v1 = s + 1 <= r ? a.scale * __uint_as_float(g[ch * 8 + 2 * i + 1]) * ex2(br - Gs[s + 1]) : 0.f;
+              v0 = s <= r ? a.scale * __uint_as_float(g[ii]) * ex2(br - fv[ii]) : 0.f;
+              v1 = s + 1 <= r ? a.scale * __uint_as_float(g[ii + 1]) * ex2(br - fv[ii + 1]) : 0.f;
             }
             ph[i] = __floats2half2_rn(v0, v1);
           }
@@ -477,26 +498,24 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
       }
     }
 
-    // ---- fp16 images of T and D T as K-major B operands: row j = T[.][j] ----
-    if (t < C) {
-      const int j = t;
+    // ---- fp16 images of T and D T as K-major B operands: row j = T[.][j];
+    //      one 16-byte chunk per task, spread over the whole warpgroup ----
+    for (int task = t; task < C * (C / 8); task += NT) {
+      const int j = task % C, ch = task / C;
       const float *trow = As + j * LDT;
-#pragma unroll
-      for (int ch = 0; ch < C / 8; ch++) {
-        const float4 t0v = *reinterpret_cast<const float4 *>(trow + ch * 8);
-        const float4 t1v = *reinterpret_cast<const float4 *>(trow + ch * 8 + 4);
-        const float4 d0 = *reinterpret_cast<const float4 *>(Ds + ch * 8);
-        const float4 d1 = *reinterpret_cast<const float4 *>(Ds + ch * 8 + 4);
-        uint4 pt, pd;
-        __half2 *ht = reinterpret_cast<__half2 *>(&pt);
-        __half2 *hd = reinterpret_cast<__half2 *>(&pd);
-        ht[0] = __floats2half2_rn(t0v.x, t0v.y); ht[1] = __floats2half2_rn(t0v.z, t0v.w);
-        ht[2] = __floats2half2_rn(t1v.x, t1v.y); ht[3] = __floats2half2_rn(t1v.z, t1v.w);
-        hd[0] = __floats2half2_rn(d0.x * t0v.x, d0.y * t0v.y); hd[1] = __floats2half2_rn(d0.z * t0v.z, d0.w * t0v.w);
-        hd[2] = __floats2half2_rn(d1.x * t1v.x, d1.y * t1v.y); hd[3] = __floats2half2_rn(d1.z * t1v.z, d1.w * t1v.w);
-        *reinterpret_cast<uint4 *>(sm + SM::QS0 + kmajor_off(j, ch * 8, 64)) = pt;
-        *reinterpret_cast<uint4 *>(sm + SM::QS1 + kmajor_off(j, ch * 8, 64)) = pd;
-      }
+      const float4 t0v = *reinterpret_cast<const float4 *>(trow + ch * 8);
+      const float4 t1v = *reinterpret_cast<const float4 *>(trow + ch * 8 + 4);
+      const float4 d0 = *reinterpret_cast<const float4 *>(Ds + ch * 8);
+      const float4 d1 = *reinterpret_cast<const float4 *>(Ds + ch * 8 + 4);
+      uint4 pt, pd;
+      __half2 *ht = reinterpret_cast<__half2 *>(&pt);
+      __half2 *hd = reinterpret_cast<__half2 *>(&pd);
+      ht[0] = __floats2half2_rn(t0v.x, t0v.y); ht[1] = __floats2half2_rn(t0v.z, t0v.w);
+      ht[2] = __floats2half2_rn(t1v.x, t1v.y); ht[3] = __floats2half2_rn(t1v.z, t1v.w);
+      hd[0] = __floats2half2_rn(d0.x * t0v.x, d0.y * t0v.y); hd[1] = __floats2half2_rn(d0.z * t0v.z, d0.w * t0v.w);
+      hd[2] = __floats2half2_rn(d1.x * t1v.x, d1.y * t1v.y); hd[3] = __floats2half2_rn(d1.z * t1v.z, d1.w * t1v.w);
+      *reinterpret_cast<uint4 *>(sm + SM::QS0 + kmajor_off(j, ch * 8, 64)) = pt;
+      *reinterpret_cast<uint4 *>(sm + SM::QS1 + kmajor_off(j, ch * 8, 64)) = pd;
     }
     fence_proxy_async();
     fence_before_sync();
