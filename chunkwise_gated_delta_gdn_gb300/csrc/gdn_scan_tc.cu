@@ -236,7 +236,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     auto issue_o_intra = [&](int cc) {  // D3 = AqkT Y[cc&1]
       const uint32_t sP = smem_addr(sm + SM::kP + (cc % NST) * SM::PI);
 #pragma unroll
-      for (int k0 = 0; k0 < 64; k0 += 16) {
+      for (int k0 = 0; k0 < C; k0 += 16) {  // K = C: rows of Y beyond C are zero
         const uint64_t bd = make_desc(sY + (cc & 1) * SM::YI + (k0 >> 4) * 2048, 8 * 1024, 1024);
         mma_f16(tD3, make_desc(sP + 64 * 128 + k0 * 2, 16, 1024), bd, idesc, k0 > 0 ? 1u : 0u);
       }
@@ -307,7 +307,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         if (c + 2 < nchunks) issue_v(c + 2);
         const uint32_t sP = smem_addr(sm + SM::kP + s * SM::PI);
 #pragma unroll
-        for (int k0 = 0; k0 < 64; k0 += 16) {
+        for (int k0 = 0; k0 < C; k0 += 16) {  // K = C: rows of Y beyond C are zero
           const uint64_t bd = make_desc(sY + (c & 1) * SM::YI + (k0 >> 4) * 2048, 8 * 1024, 1024);
           mma_f16(tD2, make_desc(sP + k0 * 2, 16, 1024), bd, idesc, k0 > 0 ? 1u : 0u);
         }
