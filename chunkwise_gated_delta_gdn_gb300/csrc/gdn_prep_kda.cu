@@ -29,8 +29,9 @@
 //   P1   = Kt^T T,  AqkT = Aqk T   (tcgen05, fp16 operands, fp32 accumulation)
 // written, rounded once to fp16, as the 24 KB image [P1; AqkT] (K-major,
 // 128-byte swizzle, 192 rows of 64 elements) with one bulk copy; the gated
-// image [Kg; Qg] (128 rows, rows past the tokens zero) and e^{b_last} per key
-// channel go straight to global memory.
+// image [Kg; Qg] (per 64-channel panel 2C rows: the keys, then the queries;
+// rows past the tokens zero) and e^{b_last} per key channel go straight to
+// global memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -50,6 +51,9 @@ constexpr int kNT = 128;   // threads
 constexpr int kRef = 16;   // reference row of the factored exponentials
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kWide = 100.f;  // largest |b_r - b_ref| (log2 units) for the factored form
+// the gated [Kg; Qg] image: per 64-channel panel, the C key rows then the C
+// query rows (128-byte rows, 128-byte swizzle)
+constexpr int kKqPanel = 2 * kC * 128;
 
 __device__ __forceinline__ float ex2k(float x) {
   float y;
@@ -241,15 +245,9 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
           kt0 = kf.x * ex2k(bl.x - b.x); kt1 = kf.y * ex2k(bl.y - b.y);
         }
         const __half2 kg = __floats2half2_rn(kg0, kg1), qg = __floats2half2_rn(qg0, qg1);
-        *reinterpret_cast<__half2 *>(kqi + p * 16384 + off) = kg;
-        *reinterpret_cast<__half2 *>(kqi + p * 16384 + 64 * 128 + off) = qg;
+        *reinterpret_cast<__half2 *>(kqi + p * kKqPanel + off) = kg;
+        *reinterpret_cast<__half2 *>(kqi + p * kKqPanel + kC * 128 + off) = qg;
         *reinterpret_cast<__half2 *>(sm + SM::kKt + p * C * 128 + off) = __floats2half2_rn(kt0, kt1);
-      }
-      // rows C..63 and 64+C..127 of the gated image: zero
-      for (int idx = tid; idx < 64 * 8; idx += kNT) {
-        const int z = idx >> 3, ch = idx & 7;
-        const int rr = z < 32 ? C + z : 64 + C + (z - 32);
-        *reinterpret_cast<uint4 *>(kqi + p * 16384 + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
       }
       if (!wide) {
         fence_proxy_async();

@@ -10,8 +10,9 @@
 //    sequence (register-resident state, stratat pull #1296, "What this is");
 //    an fp16 copy in shared memory is the B operand of the products with S.
 //    Per chunk c (C rows, P1 and AqkT from the prep kernel's image):
-//       D1[c&1] = [Kg; Qg] S          one M=128 MMA (rows 0..63 keys,
-//                                     64..127 queries), K = dk
+//       D1[c&1] = [Kg; Qg] S          one M=128 MMA (key rows from 0, query
+//                                     rows from C at chunk 32, from 64 at
+//                                     chunk 64), K = dk
 //       Y       = diag(beta)(V - D1[keys])       -> fp16 B operand Y[c&1]
 //       D2      = P1 Y                S <- diag(exp(b_last)) S + D2
 //       D3      = AqkT Y              issued right behind D2; it runs during
@@ -55,7 +56,15 @@ static_assert(NS == 64, "one 128-byte swizzle atom per S / Y row");
 
 template <int C, int DK, int NST>
 struct ScanTcSmem {
-  static constexpr int KQ = (DK / 64) * 128 * 128;  // [Kg; Qg], K-major, 128 rows
+  static constexpr int KQ = (DK / 64) * 128 * 128;  // [Kg; Qg] stage, K-major, 128 rows per panel
+  // The prep writes the image compactly at chunk 32 (per panel the C key rows,
+  // then the C query rows: query lanes C..2C-1), at chunk 64 as 128 rows with
+  // the queries from row 64; the stage keeps 128 rows per panel so that the
+  // M = 128 product never reads past it.
+  static constexpr bool COMPACT = C == 32;
+  static constexpr int Q0 = COMPACT ? C : 64;          // first query row / lane
+  static constexpr int KQP = COMPACT ? 2 * C * 128 : 128 * 128;  // bytes of one panel
+  static constexpr int KQL = (DK / 64) * KQP;          // bytes copied per chunk
   static constexpr int PI = kPrepImageBytes;         // [P1; AqkT]
   static constexpr int SI = (DK / 8) * 1024;         // S, MN-major, dk K-rows
   static constexpr int YI = 8 * 1024;                // Y, MN-major, 64 K-rows (x2)
@@ -78,7 +87,7 @@ struct ScanTcSmem {
   static constexpr int kBytes = kUsed + kSlack;
   // bytes landing per chunk: [Kg; Qg] (GDN: the prep's image; KDA: two TMA
   // boxes per panel) and the prep image
-  static constexpr uint32_t kTx = KQ + PI;
+  static constexpr uint32_t kTx = KQL + PI;
   static_assert(KQ % 1024 == 0 && PI % 1024 == 0 && SI % 1024 == 0 && VI % 1024 == 0,
                 "1024-byte operand alignment");
   static_assert(kBytes <= 232448, "shared memory budget of one CTA");
@@ -158,7 +167,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     const int c0 = hh * NH;             // first column of this thread
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const bool key_warp = q * 32 < C;                       // lanes of key rows
-    const bool query_warp = q >= 2 && (q - 2) * 32 < C;     // lanes of query rows
+    const bool query_warp = q * 32 >= SM::Q0 && q * 32 - SM::Q0 < C;  // lanes of query rows
     const bool state_warp = q * 32 < DK;
     float s_reg[NH];
     const size_t hoff = ((size_t)n * a.HV + hv) * (size_t)DK * a.dv;
@@ -209,7 +218,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
     };
     // O of chunk cc = scale gam Qg S (D1[cc&1], query lanes) + AqkT Y (D3)
     auto output_rows = [&](int cc) {
-      const int r = t - 64;
+      const int r = t - SM::Q0;
       const int t0 = start + cc * C;
       const int L = min(C, end - t0);
       float qs[NH], d[NH];
@@ -238,7 +247,10 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
 #pragma unroll
       for (int k0 = 0; k0 < C; k0 += 16) {  // K = C: rows of Y beyond C are zero
         const uint64_t bd = make_desc(sY + (cc & 1) * SM::YI + (k0 >> 4) * 2048, 8 * 1024, 1024);
-        mma_f16(tD3, make_desc(sP + 64 * 128 + k0 * 2, 16, 1024), bd, idesc, k0 > 0 ? 1u : 0u);
+        // A from image row 128 - Q0: Aqk T row r lands in lane Q0 + r, the
+        // query lane of row r (rows past the image read what follows it in
+        // shared memory and land in lanes never read)
+        mma_f16(tD3, make_desc(sP + (128 - SM::Q0) * 128 + k0 * 2, 16, 1024), bd, idesc, k0 > 0 ? 1u : 0u);
       }
       mma_commit(bar_mma3);
     };
@@ -254,7 +266,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         const uint32_t sKQ = smem_addr(sm + SM::kKQ + s * SM::KQ);
 #pragma unroll
         for (int k0 = 0; k0 < DK; k0 += 16) {
-          const uint64_t ad = make_desc(sKQ + (k0 >> 6) * 16384 + (k0 & 63) * 2, 16, 1024);
+          const uint64_t ad = make_desc(sKQ + (k0 >> 6) * SM::KQP + (k0 & 63) * 2, 16, 1024);
           const uint64_t bd = make_desc(sS + (k0 >> 4) * 2048, (DK / 8) * 1024, 1024);
           mma_f16(tD1 + (c & 1) * NS, ad, bd, idesc, k0 > 0 ? 1u : 0u);
         }
@@ -361,7 +373,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         mbar_arrive_expect_tx(full, SM::kTx);
         // the prep kernel's gated fp16 [K~; Q~] image of this chunk
         bulk_g2s(smem_addr(sm + SM::kKQ + s * SM::KQ),
-                 a.kq_images + ((size_t)(base + c) * a.HV + hv) * SM::KQ, SM::KQ, full);
+                 a.kq_images + ((size_t)(base + c) * a.HV + hv) * SM::KQ, SM::KQL, full);
         const unsigned char *src = reinterpret_cast<const unsigned char *>(a.tiles) +
                                    ((size_t)(base + c) * a.HV + hv) * kPrepImageBytes;
         bulk_g2s(smem_addr(sm + SM::kP + s * SM::PI), src, kPrepImageBytes, full);
