@@ -18,6 +18,11 @@ constexpr int kScanTcSlice = 64;
 // (rows 0..127 = P1 = Kt^T T, rows 128..191 = Aqk T).
 constexpr int kPrepImageRows = 192;
 constexpr int kPrepImageBytes = kPrepImageRows * 128;
+// At chunk 32 (per-key gate) its columns beyond C are never read: the image is
+// written as 160 rows x 32 fp16 instead (K-major with the 64-byte swizzle; rows
+// 0..127 = P1, rows 128..159 = Aqk T) in the first 10 KB of the same record.
+constexpr int kPrepImage32Rows = 160;
+constexpr int kPrepImage32Bytes = kPrepImage32Rows * 64;
 // The scalar-gate bf16 path's image (one-chunk lookahead): 256 rows x 64 fp16,
 // K-major with the 128-byte swizzle: rows 0..127 = P1 of the chunk, rows
 // 128..191 = E = K_next P1 (the next chunk's keys times this chunk's P1; zero

@@ -27,8 +27,8 @@
 //   T    = (I + A)^-1   (16 x 16 diagonal blocks by forward substitution, then
 //          the block row)
 //   P1   = Kt^T T,  AqkT = Aqk T   (tcgen05, fp16 operands, fp32 accumulation)
-// written, rounded once to fp16, as the 24 KB image [P1; AqkT] (K-major,
-// 128-byte swizzle, 192 rows of 64 elements) with one bulk copy; the gated
+// written, rounded once to fp16, as the 10 KB image [P1; AqkT] (K-major,
+// 64-byte swizzle, 160 rows of 32 elements) with one bulk copy; the gated
 // image [Kg; Qg] (per 64-channel panel 2C rows: the keys, then the queries;
 // rows past the tokens zero) and e^{b_last} per key channel go straight to
 // global memory.
@@ -95,7 +95,7 @@ struct KdaSmem {
   static constexpr int kAqkOp = kK;
   static_assert(kAqkF + kC * LDC * 4 <= kTimg, "fp32 arrays below the T image");
   static_assert(kTimg + kC * 128 <= kPl + 24576, "T image inside the planes region");
-  static_assert(kPrepImageBytes <= 24576, "output image inside the planes region");
+  static_assert(kPrepImage32Bytes <= 24576, "output image inside the planes region");
   static_assert(kPl - kK >= 16384, "the Aqk operand's 128-row span over the dead tiles");
   static_assert(kBar % 8 == 0 && kPl % 1024 == 0 && kKt % 1024 == 0, "alignment");
   static_assert(3 * (kBytes + 1024) <= 232448, "three CTAs per SM");
@@ -434,8 +434,8 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   mbar_wait(bar_mma, (wide ? 0 : NP) & 1, abort_flag);
   fence_after_sync();
 
-  // ---- the image [P1; AqkT]: row t of P1 (zero for t >= dk), rows 128 + r of
-  //      AqkT (zero for r >= C); columns >= C zero ----
+  // ---- the image [P1; AqkT], 32 columns per row in the 64-byte swizzle:
+  //      row t of P1 (zero for t >= dk), rows 128 + r of AqkT ----
   unsigned char *img = sm + SM::kImg;
   {
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
@@ -446,20 +446,20 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
         tmem_wait_ld();
       }
 #pragma unroll
-      for (int ch = 0; ch < 8; ch++) {
+      for (int ch = 0; ch < C / 8; ch++) {
         uint4 pk = make_uint4(0, 0, 0, 0);
-        if (have && ch < C / 8) {
+        if (have) {
           __half2 *hh = reinterpret_cast<__half2 *>(&pk);
 #pragma unroll
           for (int i = 0; i < 4; i++)
             hh[i] = __floats2half2_rn(__uint_as_float(v[ch * 8 + 2 * i]), __uint_as_float(v[ch * 8 + 2 * i + 1]));
         }
-        *reinterpret_cast<uint4 *>(img + kmajor_off(row, ch * 8, kPrepImageRows)) = pk;
+        *reinterpret_cast<uint4 *>(img + kmajor64_off(row, ch * 8)) = pk;
       }
     };
     // tensor-memory loads are warp-wide: every lane of a warp loads
     put_row(tid, tmem + lane_base + 32, warp * 32 < DK);
-    if (warp < 2) put_row(128 + tid, tmem + lane_base + 64, warp == 0);
+    if (warp == 0) put_row(128 + tid, tmem + lane_base + 64, true);
   }
   fence_proxy_async();
   fence_before_sync();
@@ -469,7 +469,7 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   // ---- image -> workspace, one bulk copy ----
   if (tid == 0) {
     unsigned char *dst = reinterpret_cast<unsigned char *>(a.tiles) + ((size_t)slot * a.HV + hv) * kPrepImageBytes;
-    bulk_s2g(dst, smem_addr(img), kPrepImageBytes);
+    bulk_s2g(dst, smem_addr(img), kPrepImage32Bytes);
     bulk_commit();
     bulk_wait_read_all();
     if (*abort_flag) atomicOr(a.flags, kFlagTimeout);

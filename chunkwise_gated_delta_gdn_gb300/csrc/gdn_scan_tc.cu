@@ -87,7 +87,10 @@ struct ScanTcSmem {
   static constexpr int kBytes = kUsed + kSlack;
   // bytes landing per chunk: [Kg; Qg] (GDN: the prep's image; KDA: two TMA
   // boxes per panel) and the prep image
-  static constexpr uint32_t kTx = KQL + PI;
+  // the [P1; AqkT] image: at chunk 32 its 10 KB form (32 columns per row, the
+  // 64-byte swizzle), else 192 rows of 64 columns; the slot keeps 24 KB
+  static constexpr int PL = COMPACT ? kPrepImage32Bytes : kPrepImageBytes;
+  static constexpr uint32_t kTx = KQL + PL;
   static_assert(KQ % 1024 == 0 && PI % 1024 == 0 && SI % 1024 == 0 && VI % 1024 == 0,
                 "1024-byte operand alignment");
   static_assert(kBytes <= 232448, "shared memory budget of one CTA");
@@ -250,7 +253,9 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
         // A from image row 128 - Q0: Aqk T row r lands in lane Q0 + r, the
         // query lane of row r (rows past the image read what follows it in
         // shared memory and land in lanes never read)
-        mma_f16(tD3, make_desc(sP + (128 - SM::Q0) * 128 + k0 * 2, 16, 1024), bd, idesc, k0 > 0 ? 1u : 0u);
+        const uint64_t ad = SM::COMPACT ? make_desc_sw64(sP + (128 - SM::Q0) * 64 + k0 * 2, 512)
+                                        : make_desc(sP + (128 - SM::Q0) * 128 + k0 * 2, 16, 1024);
+        mma_f16(tD3, ad, bd, idesc, k0 > 0 ? 1u : 0u);
       }
       mma_commit(bar_mma3);
     };
@@ -321,7 +326,8 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
 #pragma unroll
         for (int k0 = 0; k0 < C; k0 += 16) {  // K = C: rows of Y beyond C are zero
           const uint64_t bd = make_desc(sY + (c & 1) * SM::YI + (k0 >> 4) * 2048, 8 * 1024, 1024);
-          mma_f16(tD2, make_desc(sP + k0 * 2, 16, 1024), bd, idesc, k0 > 0 ? 1u : 0u);
+          const uint64_t ad = SM::COMPACT ? make_desc_sw64(sP + k0 * 2, 512) : make_desc(sP + k0 * 2, 16, 1024);
+          mma_f16(tD2, ad, bd, idesc, k0 > 0 ? 1u : 0u);
         }
         mma_commit(bar_mma2);
         issue_o_intra(c);
@@ -376,7 +382,7 @@ gdn_scan_tc_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
                  a.kq_images + ((size_t)(base + c) * a.HV + hv) * SM::KQ, SM::KQL, full);
         const unsigned char *src = reinterpret_cast<const unsigned char *>(a.tiles) +
                                    ((size_t)(base + c) * a.HV + hv) * kPrepImageBytes;
-        bulk_g2s(smem_addr(sm + SM::kP + s * SM::PI), src, kPrepImageBytes, full);
+        bulk_g2s(smem_addr(sm + SM::kP + s * SM::PI), src, SM::PL, full);
       }
       float *raw = reinterpret_cast<float *>(sm + SM::kRaw + s * SM::NRAW * 4);
       // the chunk's per-channel decay (from the prep kernel) and beta

@@ -51,6 +51,22 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// The same for K-major images with 64-byte rows (32 16-bit elements) in the
+// 64-byte swizzle: 8-row atoms of 512 bytes, the 16-byte chunk index inside a
+// row XORed with (row / 2) % 4.
+__device__ __forceinline__ uint32_t kmajor64_off(int row, int k) {
+  return row * 64 + (((((k * 2) >> 4) ^ (row >> 1)) & 3) << 4) + ((k * 2) & 15);
+}
+__device__ __forceinline__ uint64_t make_desc_sw64(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;  // leading-byte offset (unused by swizzled K-major operands)
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;  // 64-byte swizzle
+  return d;
+}
+
 // instruction descriptor: fp16 A and B, fp32 D, M x N, operand majorness
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
