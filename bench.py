@@ -86,26 +86,39 @@ def algorithmic_bytes(c, which="path"):
 
 # what each kernel of the split design reads and writes at least once, per
 # chunk slot: the scalar-gate bf16 path's prep writes one 32 KB operand image
-# per value head and one 32 KB [K_next; Q] image per q/k head, which the scan
-# reads back
+# per value head and one 32 KB [K_next; Q] image per q/k head, the per-key-gate
+# path's prep an operand image and a gated [Kg; Qg] image per value head, and
+# the scan reads them back
 KERNEL_BYTES_NOTE = {
     ("scan", "bf16", 0): "v, o, g, beta plus the prep's operand images read back "
                          "(HV x 32 KB and H x 32 KB per chunk)",
     ("prep", "bf16", 0): "q, k, g, beta plus the operand images written "
                          "(HV x 32 KB and H x 32 KB per chunk)",
+    ("scan", "bf16", 1): "v, o, beta plus the prep's images read back (per chunk and value "
+                         "head: [P1; AqkT] and the gated [Kg; Qg], 10 + 16 KB at chunk 32, "
+                         "24 + 32 KB at chunk 64, and dk decays)",
+    ("prep", "bf16", 1): "q, k, the per-channel g, beta plus the images written (per chunk "
+                         "and value head: 10 + 16 KB at chunk 32, 24 + 32 KB at chunk 64, and "
+                         "dk decays)",
 }
 
 
 def kernel_design_bytes(c, which, case, cu_seqlens=None):
-    """Bytes one kernel of the scalar-gate bf16 split design must move; None
-    for the other paths.  ``cu_seqlens``: the packed cuts of a varlen workload."""
+    """Bytes one kernel of the bf16 split design must move; None for the fp32
+    path.  ``cu_seqlens``: the packed cuts of a varlen workload."""
     if (which, c.dtype_name, c.gate_mode) not in KERNEL_BYTES_NOTE:
         return None
     n = c.tokens
     slots = n // c.chunk + case.num_states  # chunk slots the workspace holds (upper bound)
     chunks = sum(-(-L // c.chunk) for L in seq_lengths(case, cu_seqlens))
-    images = chunks * (c.HV * 32768 + c.H * (c.dk // 64) * 16384)
     assert chunks <= slots
+    if c.gate_mode == 1:  # per-key gate: per (chunk, value head) images and decays
+        per = (10240 + (c.dk // 64) * 8192) if c.chunk == 32 else (24576 + (c.dk // 64) * 16384)
+        images = chunks * c.HV * (per + c.dk * 4)
+        if which == "scan":
+            return 2 * n * c.HV * c.dv * 2 + n * c.HV * 4 + images
+        return 2 * n * c.H * c.dk * 2 + n * c.HV * c.dk * 4 + n * c.HV * 4 + images
+    images = chunks * (c.HV * 32768 + c.H * (c.dk // 64) * 16384)
     if which == "scan":
         return 2 * n * c.HV * c.dv * 2 + 2 * n * c.HV * 4 + images
     return 2 * n * c.H * c.dk * 2 + 2 * n * c.HV * 4 + images

@@ -99,6 +99,15 @@ def test_kernel_own_bytes_of_the_split_design():
     chunks = 2 + 1 + (131072 - 1 - 164 + 63) // 64 + 1
     assert bench.kernel_design_bytes(wv, "scan", cv, cu) == (
         131072 * (2 * 12288 + 384) + chunks * 64 * 32768)
-    # other paths have no split-design figure
+    # KDA at chunk 32: per chunk and value head a 10 KB [P1; AqkT] image, a
+    # 16 KB gated [Kg; Qg] image and 128 decays; 2 x 256 chunks, 32 value heads.
+    # The scan reads v, writes o (32*128*2 B/token each) and reads beta (32*4);
+    # the prep reads q, k (2*32*128*2), g (32*128*4) and beta.  (ncu measured
+    # 0.70 and 0.95 GB.)
     ck, wk = view("kda_bf16_b2_t8192")
-    assert bench.kernel_design_bytes(wk, "scan", ck) is None
+    images_k = 512 * 32 * (10240 + 16384 + 512)
+    assert bench.kernel_design_bytes(wk, "scan", ck) == 16384 * (2 * 8192 + 128) + images_k
+    assert bench.kernel_design_bytes(wk, "prep", ck) == 16384 * (16384 + 16384 + 128) + images_k
+    # the fp32 path has no split-design figure
+    cf, wf = view("gdn_fp32_t256")
+    assert bench.kernel_design_bytes(wf, "scan", cf) is None
