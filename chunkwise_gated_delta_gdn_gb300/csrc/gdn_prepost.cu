@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kConvThreads = 128;
 constexpr int kConvVec = 4;      // channels per thread
-constexpr int kConvTokens = 32;  // tokens per thread
+constexpr int kConvTokens = 128;  // tokens per thread (halo re-read: W - 1 of them)
 constexpr int kConvAhead = 8;    // tokens loaded ahead of use
 
 // 4 consecutive elements, raw: one 8-byte load for bf16, one 16-byte for fp32
