@@ -17,11 +17,16 @@
 //
 // The work is bound by the state's HBM traffic (read dk x dv fp32 once, write
 // it once per call); everything else is a few hundred bytes per (token, head).
-// One CTA of 256 threads owns a (sequence, value head, 32-column slice): lane
-// (w, l) holds rows w*4 + l/8 + 32 i of columns 4 (l % 8) .. +3, so every 8
+// One CTA of 128 threads owns a (sequence, value head, 32-column slice): lane
+// (w, l) holds rows w*4 + l/8 + 16 i of columns 4 (l % 8) .. +3, so every 8
 // lanes read one 128-byte row segment (coalesced float4 loads and stores), and
 // the column sums over rows reduce by two shuffles and one pass over shared
-// memory.
+// memory.  A thread holds dk/16 rows (128 bytes of state at dk = 128), and
+// seven (per-key gate, 72 registers) or eight (scalar gate, 64) CTAs fit on
+// an SM: 112-128 KB of loads in flight per SM, enough to keep HBM busy
+// through each CTA's load -> reduce -> store sequence.  With 256 threads and
+// half the rows per thread (five CTAs per SM, 80 KB) the scalar-gate decode
+// step ran at 86% of the copy bandwidth instead of 96%.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -31,20 +36,21 @@
 namespace gdn {
 namespace {
 
-constexpr int kRecThreads = 256;
+constexpr int kRecThreads = 128;
 constexpr int kRecSlice = 32;  // dv columns per CTA
 
 template <int DK, bool BF16, int GATE>
 __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArgs a) {
   using E = Elem<BF16>;
   using T = typename E::T;
-  constexpr int RPT = DK / 32;  // rows per thread
+  constexpr int NW = kRecThreads / 32;
+  constexpr int RPT = DK / (4 * NW);  // rows per thread
   const int n = blockIdx.x, hv = blockIdx.y, j0 = blockIdx.z * kRecSlice;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, cg = lane & 7;
-  const int r0 = w * 4 + (lane >> 3);  // this thread's rows: r0 + 32 i
+  const int r0 = w * 4 + (lane >> 3);  // this thread's rows: r0 + 4 NW i
   const int hq = hv / (a.HV / a.H);
 
-  __shared__ float red[8][8][9];  // [warp][column group][4 x S^T k, 4 x S^T q, k.q]
+  __shared__ float red[NW][8][9];  // [warp][column group][4 x S^T k, 4 x S^T q, k.q]
   __shared__ __align__(16) float ub[kRecSlice];
 
   int start, end;
@@ -62,7 +68,7 @@ __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArg
 #pragma unroll
   for (int i = 0; i < RPT; i++) {
     if (a.h0)
-      S[i] = *reinterpret_cast<const float4 *>(a.h0 + sbase + (size_t)(r0 + 32 * i) * a.dv);
+      S[i] = *reinterpret_cast<const float4 *>(a.h0 + sbase + (size_t)(r0 + 4 * NW * i) * a.dv);
     else
       S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -79,8 +85,8 @@ __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArg
     float kk[RPT], qq[RPT], dec[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; i++) {
-      kk[i] = E::to_f(kp[qk + 32 * i]);
-      qq[i] = E::to_f(qp[qk + 32 * i]);
+      kk[i] = E::to_f(kp[qk + 4 * NW * i]);
+      qq[i] = E::to_f(qp[qk + 4 * NW * i]);
     }
     if constexpr (GATE == 0) {
       const float gt = __ldg(a.g + th);
@@ -91,7 +97,7 @@ __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArg
     } else {
 #pragma unroll
       for (int i = 0; i < RPT; i++) {
-        const float gt = __ldg(a.g + th * DK + r0 + 32 * i);
+        const float gt = __ldg(a.g + th * DK + r0 + 4 * NW * i);
         positive |= gt > 0.f;
         dec[i] = expf(gt);
       }
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArg
       const int c = tid >> 2, e = tid & 3;
       float sk = 0.f, sq = 0.f, kq = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < 8; ww++) {
+      for (int ww = 0; ww < NW; ww++) {
         sk += red[ww][c][e];
         sq += red[ww][c][4 + e];
         kq += red[ww][0][8];
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArg
     for (int i = 0; i < RPT; i++) {
       nonfinite |= !(isfinite(S[i].x) && isfinite(S[i].y) && isfinite(S[i].z) &&
                      isfinite(S[i].w));
-      *reinterpret_cast<float4 *>(a.hT + sbase + (size_t)(r0 + 32 * i) * a.dv) = S[i];
+      *reinterpret_cast<float4 *>(a.hT + sbase + (size_t)(r0 + 4 * NW * i) * a.dv) = S[i];
     }
   }
   if (a.flags) {
