@@ -15,13 +15,13 @@
 //        y = x / sqrt(mean(x^2) + eps) * weight [* silu(z)].
 //
 // Convolution layout: one thread owns 4 adjacent channels (one 8-byte bf16
-// load per token) and walks 32 consecutive tokens, keeping the last W - 1
+// load per token) and walks 128 consecutive tokens, keeping the last W - 1
 // inputs in registers; a warp covers 128 channels of a token with coalesced
 // 256-byte accesses, and loads eight tokens ahead of use.  Four channels keep
 // the thread under 80 registers, so that enough warps share an SM to cover
-// the memory latency.  A tile re-reads
-// only its W - 1 tokens of halo.  The norms give one warp four rows, each lane
-// a contiguous piece of each, all loaded before the first is reduced.
+// the memory latency.  A tile re-reads only its W - 1 tokens of halo.  The
+// norms give each row 32 (L2) or 16 (gated RMS) lanes, each lane a contiguous
+// piece of it, and load all of a warp's rows before the first is reduced.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
