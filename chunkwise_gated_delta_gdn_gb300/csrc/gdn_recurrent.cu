@@ -18,15 +18,19 @@
 // The work is bound by the state's HBM traffic (read dk x dv fp32 once, write
 // it once per call); everything else is a few hundred bytes per (token, head).
 // One CTA of 128 threads owns a (sequence, value head, 32-column slice): lane
-// (w, l) holds rows w*4 + l/8 + 16 i of columns 4 (l % 8) .. +3, so every 8
-// lanes read one 128-byte row segment (coalesced float4 loads and stores), and
-// the column sums over rows reduce by two shuffles and one pass over shared
-// memory.  A thread holds dk/16 rows (128 bytes of state at dk = 128), and
-// seven (per-key gate, 72 registers) or eight (scalar gate, 64) CTAs fit on
-// an SM: 112-128 KB of loads in flight per SM, enough to keep HBM busy
-// through each CTA's load -> reduce -> store sequence.  With 256 threads and
-// half the rows per thread (five CTAs per SM, 80 KB) the scalar-gate decode
-// step ran at 86% of the copy bandwidth instead of 96%.
+// (w, l) holds the dk/16 consecutive rows from dk/16 (4 w + l/8) on, columns
+// 4 (l % 8) .. +3.  Every 8 lanes read one 128-byte row segment (coalesced
+// float4 loads and stores of the state), a thread's pieces of k, q and the
+// per-key gates are contiguous (16-byte loads), and the column sums over rows
+// reduce by two shuffles and one pass over shared memory.  A thread holds 128
+// bytes of state at dk = 128, and seven (per-key gate, 72 registers) or eight
+// (scalar gate, 64) CTAs fit on an SM: 112-128 KB of loads in flight per SM,
+// enough to keep HBM busy through each CTA's load -> reduce -> store
+// sequence.  Measured on one decode step of 256 sequences (dk = dv = 128):
+// with 256 threads of 4 rows each (five CTAs per SM, 80 KB) the scalar-gate
+// step ran at 86% of the copy bandwidth; with 8 rows per thread 16 rows apart
+// (scalar loads of k, q and the gates) at 96% (scalar gate) and 80% (per-key
+// gate); with the rows contiguous at 98% and 95%.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -39,6 +43,39 @@ namespace {
 constexpr int kRecThreads = 128;
 constexpr int kRecSlice = 32;  // dv columns per CTA
 
+// N consecutive elements (bf16 or fp32) as floats, in 16-byte loads (N * size a
+// multiple of 16 bytes, the address 16-byte aligned)
+template <int N, bool BF16>
+__device__ __forceinline__ void load_vec(const void *p, float (&v)[N]) {
+  if constexpr (BF16) {
+    static_assert(N % 8 == 0 || N == 4, "whole 16- or 8-byte pieces");
+    if constexpr (N % 8 == 0) {
+#pragma unroll
+      for (int i = 0; i < N; i += 8) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p) + i));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
+          v[i + 2 * j] = f.x; v[i + 2 * j + 1] = f.y;
+        }
+      }
+    } else {
+      const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+      v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+    }
+  } else {
+    static_assert(N % 4 == 0, "whole 16-byte pieces");
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const float4 f = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i));
+      v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
+    }
+  }
+}
+
 template <int DK, bool BF16, int GATE>
 __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArgs a) {
   using E = Elem<BF16>;
@@ -47,7 +84,7 @@ __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArg
   constexpr int RPT = DK / (4 * NW);  // rows per thread
   const int n = blockIdx.x, hv = blockIdx.y, j0 = blockIdx.z * kRecSlice;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, cg = lane & 7;
-  const int r0 = w * 4 + (lane >> 3);  // this thread's rows: r0 + 4 NW i
+  const int r0 = (w * 4 + (lane >> 3)) * RPT;  // this thread's rows: r0 .. r0 + RPT - 1
   const int hq = hv / (a.HV / a.H);
 
   __shared__ float red[NW][8][9];  // [warp][column group][4 x S^T k, 4 x S^T q, k.q]
@@ -68,7 +105,7 @@ __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArg
 #pragma unroll
   for (int i = 0; i < RPT; i++) {
     if (a.h0)
-      S[i] = *reinterpret_cast<const float4 *>(a.h0 + sbase + (size_t)(r0 + 4 * NW * i) * a.dv);
+      S[i] = *reinterpret_cast<const float4 *>(a.h0 + sbase + (size_t)(r0 + i) * a.dv);
     else
       S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -83,11 +120,8 @@ __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArg
     const size_t qk = ((size_t)t * a.H + hq) * DK + r0;
     const size_t th = (size_t)t * a.HV + hv;
     float kk[RPT], qq[RPT], dec[RPT];
-#pragma unroll
-    for (int i = 0; i < RPT; i++) {
-      kk[i] = E::to_f(kp[qk + 4 * NW * i]);
-      qq[i] = E::to_f(qp[qk + 4 * NW * i]);
-    }
+    load_vec<RPT, BF16>(kp + qk, kk);
+    load_vec<RPT, BF16>(qp + qk, qq);
     if constexpr (GATE == 0) {
       const float gt = __ldg(a.g + th);
       positive |= gt > 0.f;
@@ -95,11 +129,12 @@ __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArg
 #pragma unroll
       for (int i = 0; i < RPT; i++) dec[i] = d;
     } else {
+      float gt[RPT];
+      load_vec<RPT, false>(a.g + th * DK + r0, gt);
 #pragma unroll
       for (int i = 0; i < RPT; i++) {
-        const float gt = __ldg(a.g + th * DK + r0 + 4 * NW * i);
-        positive |= gt > 0.f;
-        dec[i] = expf(gt);
+        positive |= gt[i] > 0.f;
+        dec[i] = expf(gt[i]);
       }
     }
     const float bt = __ldg(a.beta + th);
@@ -165,7 +200,7 @@ __global__ void __launch_bounds__(kRecThreads) gdn_recurrent_kernel(RecurrentArg
     for (int i = 0; i < RPT; i++) {
       nonfinite |= !(isfinite(S[i].x) && isfinite(S[i].y) && isfinite(S[i].z) &&
                      isfinite(S[i].w));
-      *reinterpret_cast<float4 *>(a.hT + sbase + (size_t)(r0 + 4 * NW * i) * a.dv) = S[i];
+      *reinterpret_cast<float4 *>(a.hT + sbase + (size_t)(r0 + i) * a.dv) = S[i];
     }
   }
   if (a.flags) {
