@@ -95,6 +95,7 @@ struct ConvArgs {
   SeqInfo seq;
   int D;
   uint32_t *flags;             // device status word, or nullptr
+  int tile0 = 0;               // first token tile of this launch (set by the launcher)
 };
 struct RowNormArgs {
   const void *x, *z;           // z: gate rows (gated RMS norm only), or nullptr

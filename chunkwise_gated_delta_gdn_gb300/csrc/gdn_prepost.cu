@@ -108,7 +108,11 @@ __device__ bool seqlens_ok(const SeqInfo &s) {
   return true;
 }
 
-template <int W, bool BF16, bool SILU>
+// SPLIT: the launch covers the token tiles from a.tile0 on (inputs of more
+// than 65535 tiles, the grid's y extent, take several launches); the common
+// form keeps the tile index a pure function of blockIdx.y, which compiles
+// to faster code
+template <int W, bool BF16, bool SILU, bool SPLIT>
 __global__ void __launch_bounds__(kConvThreads) gdn_conv1d_kernel(ConvArgs a) {
   __shared__ int ok_s;
   if (threadIdx.x == 0) ok_s = seqlens_ok(a.seq) ? 1 : 0;
@@ -119,7 +123,7 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv1d_kernel(ConvArgs a) {
     return;
   }
   const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * kConvVec;
-  const int tt0 = blockIdx.y * kConvTokens;
+  const int tt0 = SPLIT ? (a.tile0 + (int)blockIdx.y) * kConvTokens : (int)blockIdx.y * kConvTokens;
   if (c0 >= a.D || tt0 >= a.seq.Ttot) return;
   const int tt1 = min(tt0 + kConvTokens, a.seq.Ttot);
   constexpr int H = W - 1;  // history length
@@ -351,13 +355,21 @@ __global__ void __launch_bounds__(256) gdn_rownorm_kernel(RowNormArgs a) {
 
 template <int W, bool BF16>
 cudaError_t conv_w(const ConvArgs &a, int act, cudaStream_t s) {
-  const dim3 grid((a.D / kConvVec + kConvThreads - 1) / kConvThreads,
-                  (a.seq.Ttot + kConvTokens - 1) / kConvTokens);
-  if (a.seq.Ttot > 0) {
-    if (act)
-      gdn_conv1d_kernel<W, BF16, true><<<grid, kConvThreads, 0, s>>>(a);
+  // token tiles on the grid's y axis, at most 65535 per launch (one launch
+  // below 8.4 M tokens)
+  const long tiles = ((long)a.seq.Ttot + kConvTokens - 1) / kConvTokens;
+  const bool split = tiles > 65535;
+  for (long t0 = 0; t0 < tiles; t0 += 65535) {
+    ConvArgs b = a;
+    b.tile0 = (int)t0;
+    const dim3 grid((a.D / kConvVec + kConvThreads - 1) / kConvThreads,
+                    (unsigned)(tiles - t0 < 65535 ? tiles - t0 : 65535));
+    if (split)
+      (act ? gdn_conv1d_kernel<W, BF16, true, true> : gdn_conv1d_kernel<W, BF16, false, true>)
+          <<<grid, kConvThreads, 0, s>>>(b);
     else
-      gdn_conv1d_kernel<W, BF16, false><<<grid, kConvThreads, 0, s>>>(a);
+      (act ? gdn_conv1d_kernel<W, BF16, true, false> : gdn_conv1d_kernel<W, BF16, false, false>)
+          <<<grid, kConvThreads, 0, s>>>(b);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -416,6 +428,7 @@ cudaError_t launch_conv1d(const ConvArgs &a, int width, int activation, int dtyp
 cudaError_t launch_rownorm(const RowNormArgs &a, int dim, int kind, int dtype,
                            cudaStream_t stream) {
   if (a.rows <= 0) return cudaSuccess;
+  if (a.rows > 16L * 0x7fffffffL) return cudaErrorInvalidValue;  // grid.x extent
   return dtype == 1 ? rows_dt<true>(a, dim, kind, stream) : rows_dt<false>(a, dim, kind, stream);
 }
 

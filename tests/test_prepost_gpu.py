@@ -110,6 +110,35 @@ def test_conv_in_place_history_and_decode_steps():
     check(h, h_ref, torch.float32, "stepped history")
 
 
+def test_conv_beyond_grid_y_extent():
+    """More token tiles (128 tokens each) than a grid's y extent of 65535: a
+    block takes every 65535th tile.  Two packed sequences; windows at the
+    start, across the sequence boundary, past the 65535th tile and at the end
+    against the oracle, and both final histories (raw inputs, exact)."""
+    D, W = 8, 4
+    T = 65535 * 128 + 1000
+    cut = 4_000_000
+    x, w, b, h0, cu = conv_inputs([cut, T - cut], D, W, torch.bfloat16, seed=11)
+    y, hT = run_conv(x, w, b, h0, cu, gdn.GDN_ACT_SILU)
+    y, xs = y[0].cpu(), x[0]
+    bounds = cu.tolist()
+    for a0, a1 in ((0, 300), (cut - 150, cut + 150), (65535 * 128 - 100, 65535 * 128 + 400), (T - 300, T)):
+        parts, hists, cuts = [], [], [0]
+        for n in range(len(bounds) - 1):
+            s, e = bounds[n], bounds[n + 1]
+            lo, hi = max(a0, s), min(a1, e)
+            if lo >= hi:
+                continue
+            ext = torch.cat([h0[n], xs[s:lo].float().T], 1) if lo - s < W - 1 else xs[lo - (W - 1):lo].float().T
+            parts.append(xs[lo:hi])
+            hists.append(ext[:, ext.shape[1] - (W - 1):])
+            cuts.append(cuts[-1] + hi - lo)
+        y_ref, _ = prepost.causal_conv1d(torch.cat(parts), w, b, torch.stack(hists), cuts, 1)
+        check(y[a0:a1], y_ref, torch.bfloat16, f"y[{a0}:{a1}]")
+    h_ref = torch.stack([xs[e - (W - 1):e].float().T for e in bounds[1:]])
+    assert torch.equal(hT.cpu(), h_ref)
+
+
 def test_conv_bad_seqlens_flagged():
     x, w, b, h0, _ = conv_inputs([10, 10], 64, 4, torch.bfloat16, seed=9)
     bad = torch.tensor([0, 15, 12], dtype=torch.int32).cuda()
