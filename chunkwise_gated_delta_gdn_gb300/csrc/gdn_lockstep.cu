@@ -47,7 +47,7 @@ gdn_lockstep_kernel(const PrepArgs pa, const ScanArgs sa, const __grid_constant_
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
   if (blockIdx.x < (unsigned)n_scan) {
-    scan_la_block<C, DK>(sa, maps, blockIdx.x, sm, ready);
+    scan_la_block<C, DK, true>(sa, maps, blockIdx.x, sm, ready);
     return;
   }
   // ---- prep CTA: three warpgroups, each its own slice and 128 columns ----

@@ -103,6 +103,7 @@ struct LaSmem {
     NBAR = B_VFULL + NV
   };
   static constexpr int kMisc = kBar + NBAR * 8;
+  static constexpr int kUnits = kMisc + 12;  // lockstep: prep units published ready
   static constexpr int kUsed = kMisc + 16;
   // request 1 KB of alignment slack when it fits; otherwise the kernel checks
   // that the dynamic shared memory it received is already 1 KB aligned
@@ -114,28 +115,41 @@ struct LaSmem {
   static_assert(kBytes <= 232448, "shared memory budget of one CTA");
 };
 
-// Bounded wait for a ready flag set by the lockstep kernel's prep warpgroups
-// (release / acquire at gpu scope); false once the clock budget runs out or
-// another wait of the block gave up.
-__device__ __forceinline__ bool wait_ready(const int *flag, volatile int *abort) {
-  if (load_acquire_gpu(flag)) return true;
+// "Units 0 .. n - 1 are ready" in a shared-memory word, written by the
+// coefficient warp after its gpu-scope acquire of each unit's flag (release /
+// acquire at CTA scope), so that the threads that issue the bulk copies wait
+// on shared memory instead of an L2 round trip each.
+__device__ __forceinline__ void publish_units(uint32_t word, int n) {
+  asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(word), "r"(n) : "memory");
+}
+__device__ __forceinline__ int units_ready(uint32_t word) {
+  int n;
+  asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(n) : "r"(word) : "memory");
+  return n;
+}
+// Bounded wait until unit j is published; false once the clock budget runs
+// out or another wait of the block gave up.
+__device__ __forceinline__ bool wait_unit(uint32_t word, int j, volatile int *abort) {
+  if (units_ready(word) > j) return true;
   const long long t0 = clock64();
   while (true) {
     if (*abort) return false;
-    if (load_acquire_gpu(flag)) return true;
+    if (units_ready(word) > j) return true;
     if (clock64() - t0 > 4000000000LL) {
       *abort = 1;
       return false;
     }
-    __nanosleep(100);
   }
 }
 
 // The scan of one block (sequence, value head, dv slice) of the grid, run by
-// 384 threads on the LaSmem layout at `sm` (1 KB aligned).  With `ready`
-// given (the lockstep kernel), every prep image is loaded only once its
-// (chunk slot, q/k head) flag is set; the arithmetic is the same either way.
-template <int C, int DK>
+// 384 threads on the LaSmem layout at `sm` (1 KB aligned).  With LOCK (the
+// lockstep kernel, `ready` its flags), every prep image is loaded only once
+// its (chunk slot, q/k head) flag is set: the coefficient warp acquires the
+// flags and publishes them in shared memory for the threads that issue the
+// copies.  Without LOCK (the split kernel) none of that code exists; the
+// arithmetic is the same either way.
+template <int C, int DK, bool LOCK = false>
 __device__ __forceinline__ void scan_la_block(const ScanArgs &a, const ScanMaps &maps,
                                               int block, unsigned char *sm, const int *ready) {
   using SM = LaSmem<C, DK>;
@@ -184,6 +198,7 @@ __device__ __forceinline__ void scan_la_block(const ScanArgs &a, const ScanMaps 
     mbar_init(bar(SM::B_SREADY), kChain / 32);
     mbar_init(bar(SM::B_YREADY), kKeyWarps);
     *abort_flag = 0;
+    if constexpr (LOCK) publish_units(smem_addr(sm + SM::kUnits), 0);
     mbar_fence_init();
   }
   constexpr uint32_t kTmemCols = 512;  // D1 x3, D2, D3 x2: 6 x NS columns
@@ -386,8 +401,8 @@ __device__ __forceinline__ void scan_la_block(const ScanArgs &a, const ScanMaps 
         tma_load_3d(smem_addr(sm + SM::kV + (cc % SM::NV) * SM::VI), &maps.v, col0, hv, start + cc * C, b);
       };
       auto issue_p = [&](int j) {  // prep image of chunk j -> slot j % NP
-        if (ready) {
-          wait_ready(ready + (size_t)(base + j) * a.H + hq, abort_flag);
+        if constexpr (LOCK) {
+          wait_unit(smem_addr(sm + SM::kUnits), j, abort_flag);
           fence_proxy_async_global();
         }
         const uint32_t b = bar(SM::B_PFULL + j % NP);
@@ -507,10 +522,49 @@ __device__ __forceinline__ void scan_la_block(const ScanArgs &a, const ScanMaps 
       if (lane == 0) cf[3 * C] = __expf(blast);
       mbar_arrive(bar(SM::B_CFREADY + s));
     };
-    for (int c = 0; c < NCF - 1 && c < nch; c++) issue_cf(c);
-    for (int c = 0; c < nch; c++) {
-      finish_cf(c);
-      if (c + NCF - 1 < nch) issue_cf(c + NCF - 1);
+    if constexpr (!LOCK) {
+      for (int c = 0; c < NCF - 1 && c < nch; c++) issue_cf(c);
+      for (int c = 0; c < nch; c++) {
+        finish_cf(c);
+        if (c + NCF - 1 < nch) issue_cf(c + NCF - 1);
+      }
+    } else {
+      // lockstep: unit j (the prep images of chunk j) must be published
+      // before its bulk copies, units 0..2 first and then j + 3 with the
+      // coefficients of chunk j, about two chunks ahead.  When it is not yet,
+      // the 32 lanes each acquire the flag of one of the next 32 units and the
+      // ready prefix is published at once: one L2 round trip for up to 32
+      // units.
+      const uint32_t units_word = smem_addr(sm + SM::kUnits);
+      int published = 0;
+      auto relay = [&](int j) {
+        if (j >= nch) return;
+        const long long t0 = clock64();
+        while (published <= j) {
+          if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;  // uniform across the warp
+          const int u = published + lane;
+          const bool set = u >= nch || load_acquire_gpu(ready + (size_t)(base + u) * a.H + hq) != 0;
+          const unsigned unset = __ballot_sync(0xffffffffu, !set);
+          __syncwarp();  // the lanes' acquires before lane 0's release
+          const int n = min(published + (unset ? __ffs(unset) - 1 : 32), nch);
+          if (n > published) {
+            published = n;
+            if (lane == 0) publish_units(units_word, n);
+          } else if (clock64() - t0 > 4000000000LL) {
+            if (lane == 0) *abort_flag = 1;
+            __syncwarp();
+          } else {
+            __nanosleep(100);
+          }
+        }
+      };
+      for (int j = 0; j < 3; j++) relay(j);
+      for (int c = 0; c < NCF - 1 && c < nch; c++) issue_cf(c);
+      for (int c = 0; c < nch; c++) {
+        finish_cf(c);
+        if (c + NCF - 1 < nch) issue_cf(c + NCF - 1);
+        relay(c + 3);
+      }
     }
   } else {
     // =====================================================================
@@ -526,8 +580,8 @@ __device__ __forceinline__ void scan_la_block(const ScanArgs &a, const ScanMaps 
         const uint32_t b = bar(SM::B_KQFULL + s);
         const uint32_t kq = smem_addr(sm + SM::kKQ + s * SM::KQ);
         if (e > 0) {
-          if (ready) {
-            wait_ready(ready + (size_t)(base + e - 1) * a.H + hq, abort_flag);
+          if constexpr (LOCK) {
+            wait_unit(smem_addr(sm + SM::kUnits), e - 1, abort_flag);
             fence_proxy_async_global();
           }
           mbar_arrive_expect_tx(b, SM::KQ);
