@@ -36,7 +36,8 @@
 //    Y is double-buffered (MMA2(c) may still read Y_{c-1} while Y_c is
 //    written) and D1 triple-buffered (the query lanes read it one chunk late).
 //  * warp 9: gates and beta by cp.async, cumulative gates and the per-row
-//    coefficients (a four-deep ring).
+//    coefficients (a four-deep ring); in the lockstep kernel also the prep
+//    units' ready flags, acquired ahead and published in shared memory.
 //  * warps 10-11: the [K_{c+1}; Q_c] operand (a two-deep ring): bulk copies of
 //    the prep kernel's fp16 image; the first chunk's [K_0; Q_0] by TMA of the
 //    bf16 tiles, converted in place.
