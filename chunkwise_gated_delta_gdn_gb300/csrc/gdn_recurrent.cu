@@ -43,8 +43,8 @@ namespace {
 constexpr int kRecThreads = 128;
 constexpr int kRecSlice = 32;  // dv columns per CTA
 
-// N consecutive elements (bf16 or fp32) as floats, in 16-byte loads (N * size a
-// multiple of 16 bytes, the address 16-byte aligned)
+// N consecutive elements (bf16 or fp32) as floats, in 16-byte loads (one
+// 8-byte load for 4 bf16 elements); the address aligned to the load's size
 template <int N, bool BF16>
 __device__ __forceinline__ void load_vec(const void *p, float (&v)[N]) {
   if constexpr (BF16) {
