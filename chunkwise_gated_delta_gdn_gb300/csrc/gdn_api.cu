@@ -175,12 +175,6 @@ namespace {
 
 enum Stage { kPrep = 1, kScan = 2, kBoth = 3, kLockstep = 4 };
 
-// The lockstep launch's prep head start: the split prep kernel covers this
-// fraction of the chunk slots on every SM before the cooperative launch, whose
-// prep warpgroups (on the SMs the scan leaves) take the rest while the scan
-// walks the chunks.
-constexpr double kLockstepHead = 0.5;
-
 gdn_status run(int stages, const void *q, const void *k, const void *v, const float *g,
                const float *beta, const float *h0, void *o, float *hT,
                const int32_t *cu_seqlens, int n_seqs, int B, int T, int H, int HV, int dk,
@@ -263,8 +257,8 @@ gdn_status run(int stages, const void *q, const void *k, const void *v, const fl
     sa.o = o; sa.hT = hT; sa.seq = seq; sa.H = H; sa.HV = HV; sa.dv = dv;
     sa.scale = scale; sa.tiles = tiles; sa.flags = flags; sa.kq_images = kq_images;
     sa.decays = decays;
-    const int head = (int)((double)p.n_slots * kLockstepHead);
-    const cudaError_t e = gdn::launch_lockstep(pa, sa, maps, ready, head, chunk, dk, stream);
+    // the prep's head start is chosen by the launcher
+    const cudaError_t e = gdn::launch_lockstep(pa, sa, maps, ready, -1, chunk, dk, stream);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
       (void)cudaGetLastError();
       return GDN_ERR_UNSUPPORTED;

@@ -159,7 +159,8 @@ cudaError_t launch_scan_la(const ScanArgs &a, const ScanMaps &maps, int chunk, i
 // prep image once the prep has set its (chunk slot, q/k head) flag in
 // `ready` (n_slots x H ints, zeroed beforehand); the prep warpgroups take the
 // units from slot `head_slots` on (the earlier ones come from a prep launch
-// over the first head_slots slots, enqueued just before);
+// over the first head_slots slots, enqueued just before; head_slots < 0:
+// chosen from the problem's shape);
 // cudaErrorCooperativeLaunchTooLarge when the scan's blocks leave no SM for
 // the prep
 cudaError_t launch_lockstep(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &maps,

@@ -96,8 +96,27 @@ cudaError_t launch_one(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &m
   const long n_scan = (long)sa.seq.n_seqs * sa.HV * (sa.dv / kScanTcSlice);
   const long resident = (long)n_sm * per_sm;
   if (per_sm < 1 || n_scan + 1 > resident) return cudaErrorCooperativeLaunchTooLarge;
-  // the head start: the split prep kernel over the first head_slots slots
-  head_slots = head_slots < 0 ? 0 : (head_slots > pa.n_slots ? pa.n_slots : head_slots);
+  // The head start: the split prep kernel over the first head_slots slots.
+  // The cooperative launch's prep warpgroups ((n_sm - n_scan) x 3) must
+  // finish the other units while the scan walks its chain; measured on this
+  // GPU, one chunk step of the scan takes about kStepPerUnit of a prep unit
+  // at three per SM (1.2 against 24 us).  The head start runs in whole waves
+  // of the split prep (n_sm x 3 CTAs at once), so it is rounded up to one.
+  // At 32k tokens (H = 16, 96 scan blocks) this covers half of the slots, at
+  // 4096 tokens 0.88 of them; the swept optima were 0.5 and 0.7-0.88.
+  if (head_slots < 0) {
+    constexpr double kStepPerUnit = 0.05;
+    constexpr long kPrepPerSm = 3;  // split prep CTAs per SM
+    const long units = (long)pa.n_slots * pa.H;
+    const long chain = pa.seq.cu ? ((long)pa.seq.Ttot + (long)C * pa.seq.n_seqs - 1) / ((long)C * pa.seq.n_seqs)
+                                 : ((long)pa.seq.T + C - 1) / C;
+    const long groups = (resident - n_scan) * kPrepGroups;
+    const long need = units - (long)((double)groups * (double)chain * kStepPerUnit);
+    const long wave = (long)n_sm * kPrepPerSm;
+    const long head_units = need <= 0 ? 0 : (need + wave - 1) / wave * wave;
+    head_slots = (int)((head_units + pa.H - 1) / pa.H);
+  }
+  head_slots = head_slots > pa.n_slots ? pa.n_slots : head_slots;
   if (head_slots > 0 &&
       (err = launch_prep_tmem(pa, maps, C, DK, stream, head_slots, ready)) != cudaSuccess)
     return err;
