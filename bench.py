@@ -599,8 +599,9 @@ def main():
             "lockstep": ({"unavailable": lock_refused} if lock_refused else None) if lock_ms is None else {
                 "value": whole_job_rate(tokens_per_rank, lock_ms, world), "unit": UNIT,
                 "ms_per_step": lock_ms,
-                "note": "gdn_chunk_fwd_lockstep (the prep's first half of the chunks, then prep "
-                        "and scan in one cooperative launch), one call after another"},
+                "note": "gdn_chunk_fwd_lockstep (a prep launch over the first chunks as a head "
+                        "start, then prep and scan in one cooperative launch), one call after "
+                        "another"},
             "single_call": {"value": whole_job_rate(tokens_per_rank, single_ms, world),
                             "unit": UNIT, "ms_per_step": single_ms,
                             "note": "one gdn_chunk_fwd after another on one stream, no batches "
