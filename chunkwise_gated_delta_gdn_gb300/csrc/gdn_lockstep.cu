@@ -101,9 +101,11 @@ cudaError_t launch_one(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &m
   // finish the other units while the scan walks its chain; measured on this
   // GPU, one chunk step of the scan takes about kStepPerUnit of a prep unit
   // at three per SM (1.2 against 24 us).  The head start runs in whole waves
-  // of the split prep (n_sm x 3 CTAs at once), so it is rounded up to one.
-  // At 32k tokens (H = 16, 96 scan blocks) this covers half of the slots, at
-  // 4096 tokens 0.88 of them; the swept optima were 0.5 and 0.7-0.88.
+  // of the split prep (n_sm x 3 CTAs at once), so its units are rounded up to
+  // a wave and its slots down (a few more units in the next wave would cost a
+  // whole unit's time).  At 32k tokens (H = 16, 96 scan blocks) this covers
+  // half of the slots, at 4096 tokens 0.88 of them; the swept optima were 0.5
+  // and 0.7-0.88.
   if (head_slots < 0) {
     constexpr double kStepPerUnit = 0.05;
     constexpr long kPrepPerSm = 3;  // split prep CTAs per SM
@@ -114,7 +116,7 @@ cudaError_t launch_one(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &m
     const long need = units - (long)((double)groups * (double)chain * kStepPerUnit);
     const long wave = (long)n_sm * kPrepPerSm;
     const long head_units = need <= 0 ? 0 : (need + wave - 1) / wave * wave;
-    head_slots = (int)((head_units + pa.H - 1) / pa.H);
+    head_slots = (int)(head_units / pa.H);
   }
   head_slots = head_slots > pa.n_slots ? pa.n_slots : head_slots;
   if (head_slots > 0 &&
