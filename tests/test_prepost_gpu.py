@@ -174,6 +174,32 @@ def test_rmsnorm_gated(dtype, dim, gated):
     check(y, prepost.rmsnorm_gated(x, wt, z, 1e-6), dtype, "rmsnorm")
 
 
+@pytest.mark.parametrize("dim", [64, 128, 256])
+def test_rmsnorm_gated_odd_row_counts(dim):
+    """The gated RMS norm gives two rows side by side to each warp: with an odd
+    row count one half of the last warp has no row (zeros in, nothing stored)."""
+    g = gen(50 + dim)
+    wt = torch.rand(dim, generator=g) + 0.5
+    for rows in (1, 3, 17, 601):
+        x = (torch.randn((rows, dim), generator=g) * 2).to(torch.bfloat16)
+        z = torch.randn((rows, dim), generator=g).to(torch.bfloat16)
+        y = torch.full((rows + 1, dim), 7.0, dtype=torch.bfloat16, device="cuda")
+        gdn.gdn_rmsnorm_gated_fwd(x.cuda(), wt.cuda(), z.cuda(), eps=1e-6, y=y[:rows])
+        torch.cuda.synchronize()
+        # every element within one bf16 rounding of the exact value (plus fp32
+        # accumulation); a flat Frobenius bound is a statistic that a handful
+        # of rows can exceed even when correctly rounded, so the Frobenius error
+        # is held to that of rounding the oracle's own output instead
+        ref = np.asarray(prepost.rmsnorm_gated(x, wt, z, 1e-6), dtype=np.float64)
+        got = y[:rows].double().cpu().numpy()
+        assert np.isfinite(got).all()
+        assert (np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5).all(), f"rows={rows}"
+        rounded = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+        fro = lambda a: np.linalg.norm(a - ref) / np.linalg.norm(ref)
+        assert fro(got) <= fro(rounded) + 1e-4, (rows, fro(got), fro(rounded))
+        assert torch.all(y[rows] == 7.0), "a row past the end was written"
+
+
 def test_norms_on_empty_input():
     x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
     assert gdn.gdn_l2norm_fwd(x).numel() == 0
