@@ -64,45 +64,59 @@ __device__ __forceinline__ float ex2k(float x) {
 template <int DK>
 struct KdaSmem {
   static constexpr int NP = DK / 64;  // 64-channel panels
+  // dk = 128 builds the factored planes per 32-channel half panel (64-byte
+  // swizzle, 12 KB) and puts the solve's fp32 T and scratch over the gate
+  // tile once it is dead, so that four CTAs share an SM; dk = 64 fits four
+  // with whole-panel planes
+  static constexpr bool HALF = DK == 128;
+  static constexpr int NH = HALF ? 2 * NP : NP;  // plane products per unit
   // TMA tiles: K and Q bf16 (C rows x 128 bytes per panel, 128-byte swizzle),
   // gates fp32 (C rows x 256 bytes per panel), summed in place
   static constexpr int kK = 0;
   static constexpr int kQ = kK + NP * kC * 128;
   static constexpr int kG = kQ + NP * kC * 128;
-  // the factored operands of one panel (K-major, 128-byte swizzle):
-  // [K~; Q~] hi and lo (64 rows each), K^ hi and lo (32 rows each)
+  // the factored operands of one panel (K-major): [K~; Q~] hi and lo (64 rows
+  // each), K^ hi and lo (32 rows each); 128-byte rows (whole panel) or 64-byte
+  // rows (half panel)
   static constexpr int kPl = kG + NP * kC * 256;
-  static constexpr int PL_AH = 0, PL_AL = 8192, PL_BH = 16384, PL_BL = 20480;
+  static constexpr int ROWB = HALF ? 64 : 128;
+  static constexpr int PL_AH = 0, PL_AL = 64 * ROWB, PL_BH = 128 * ROWB, PL_BL = 160 * ROWB;
+  static constexpr int PLANES = 192 * ROWB;
   // Kt as fp16 token rows, two 64-channel panels (P1's M = 128 reads both)
-  static constexpr int kKt = kPl + 24576;
+  static constexpr int kKt = kPl + PLANES;
   static constexpr int kBeta = kKt + 2 * kC * 128;
   static constexpr int kBar = kBeta + kC * 4;  // TMA tiles, products
   static constexpr int kTslot = kBar + 16;
   static constexpr int kAbort = kTslot + 4;
   static constexpr int kMeta = kAbort + 4;
   static constexpr int kBytes = kMeta + 16 + 1024;
-  // once the A / Aqk product has read the planes, their region holds fp32 A,
-  // T and the solve's scratch (and, on the strong-decay path, fp32 Aqk), the
-  // fp16 T image (B operand), then the output image; the fp16 Aqk operand
-  // (A of a M = 128 product: 16 KB from its base) lies over the dead tiles
+  // once the A / Aqk products have read the planes, their region holds fp32 A
+  // (and, on the strong-decay path, fp32 Aqk), then the fp16 T image (B
+  // operand), then the output image; fp32 T and the solve's scratch lie over
+  // the dead gate tile (half panels) or in the plane region after A; the fp16
+  // Aqk operand (A of a M = 128 product: 16 KB from its base) lies over the
+  // dead K / Q tiles
   static constexpr int LDC = kC + 4;
+  static constexpr int ARR = kC * LDC * 4;  // one C x C fp32 array
   static constexpr int kAs = kPl;
-  static constexpr int kTs = kAs + kC * LDC * 4;
-  static constexpr int kRs = kTs + kC * LDC * 4;
-  static constexpr int kAqkF = kRs + 16 * LDC * 4;
-  static constexpr int kTimg = kPl + 16384;
+  static constexpr int kTs = HALF ? kG : kAs + ARR;
+  static constexpr int kRs = kTs + ARR;
+  static constexpr int kAqkF = HALF ? kAs + ARR : kRs + 16 * LDC * 4;
+  static constexpr int kTimg = HALF ? kPl : kPl + 16384;
   static constexpr int kImg = kPl;
   static constexpr int kAqkOp = kK;
-  static_assert(kAqkF + kC * LDC * 4 <= kTimg, "fp32 arrays below the T image");
-  static_assert(kTimg + kC * 128 <= kPl + 24576, "T image inside the planes region");
-  static_assert(kPrepImage32Bytes <= 24576, "output image inside the planes region");
+  static_assert(kAqkF + ARR <= kPl + PLANES, "fp32 A and Aqk inside the plane region");
+  static_assert(!HALF || kRs + 16 * LDC * 4 <= kPl, "T and scratch inside the dead gate tile");
+  static_assert(HALF || kAqkF + ARR <= kTimg, "fp32 arrays below the T image");
+  static_assert(kTimg + kC * 128 <= kPl + PLANES, "T image inside the planes region");
+  static_assert(kPrepImage32Bytes <= PLANES, "output image inside the planes region");
   static_assert(kPl - kK >= 16384, "the Aqk operand's 128-row span over the dead tiles");
   static_assert(kBar % 8 == 0 && kPl % 1024 == 0 && kKt % 1024 == 0, "alignment");
-  static_assert(3 * (kBytes + 1024) <= 232448, "three CTAs per SM");
+  static_assert(4 * (kBytes + 1024) <= 232448, "four CTAs per SM");
 };
 
 template <int DK>
-__global__ void __launch_bounds__(kNT, 3)
+__global__ void __launch_bounds__(kNT, 4)
 gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   using SM = KdaSmem<DK>;
   constexpr int NP = SM::NP, C = kC, LDC = SM::LDC;
@@ -192,8 +206,92 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   if (__syncthreads_or(positive) && tid == 0) atomicOr(a.flags, kFlagPositiveGate);
   wide = __syncthreads_or(wide);
 
-  // ---- one pass over the tile per 64-channel panel: factored planes (and,
-  //      per panel, their product), the gated image, Kt, the decays ----
+  // ---- one pass over the tile per 64-channel panel (dk = 64) or 32-channel
+  //      half panel (dk = 128): factored planes (and their product), the
+  //      gated image, Kt, the decays ----
+  if constexpr (SM::HALF) {
+    // 32-channel half panels hp: 16 channel pairs x 8 groups of 4 rows; the
+    // planes in the 64-byte swizzle, one K = 32 product per half panel
+    const int pp = tid & 15, rg = tid >> 4;
+    unsigned char *kqi = a.kq_images + ((size_t)slot * a.HV + hv) * kq_image_bytes(DK);
+    const uint32_t sPl = smem_addr(sm + SM::kPl);
+#pragma unroll 1
+    for (int hp = 0; hp < SM::NH; hp++) {
+      const int p = hp >> 1, col = 32 * (hp & 1) + 2 * pp;  // first channel of the pair in the panel
+      const int kc = col & 31;                                 // and in the half panel
+      if (!wide && hp > 0) {  // the previous half panel's products have read the planes
+        mbar_wait(bar_mma, (hp - 1) & 1, abort_flag);
+        fence_after_sync();
+      }
+      const float *gp = reinterpret_cast<const float *>(sm + SM::kG + p * C * 256);
+      const float2 bm = *reinterpret_cast<const float2 *>(gp + kRef * 64 + col);
+      const float2 bl = *reinterpret_cast<const float2 *>(gp + (C - 1) * 64 + col);
+      const float ebm0 = ex2k(bm.x), ebm1 = ex2k(bm.y);
+      const float elt0 = ex2k(bl.x - bm.x), elt1 = ex2k(bl.y - bm.y);
+      if (rg == 0)
+        *reinterpret_cast<float2 *>(a.decays + ((size_t)slot * a.HV + hv) * DK + p * 64 + col) =
+            make_float2(ex2k(bl.x), ex2k(bl.y));
+#pragma unroll 2
+      for (int i = 0; i < 4; i++) {
+        const int r = 4 * rg + i;
+        // element (r, col) of a 64-channel K-major row in the 128-byte swizzle,
+        // and (r, kc) of a 32-channel row in the 64-byte swizzle
+        const uint32_t off = r * 128 + ((((col >> 3) ^ (r & 7)) << 4) | ((col & 7) * 2));
+        const float2 b = *reinterpret_cast<const float2 *>(gp + r * 64 + col);
+        const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm + SM::kK + p * C * 128 + off));
+        const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm + SM::kQ + p * C * 128 + off));
+        float kg0, kg1, qg0, qg1, kt0, kt1;
+        if (!wide) {
+          const float e0 = ex2k(b.x - bm.x), e1 = ex2k(b.y - bm.y);
+          const float i0 = ex2k(bm.x - b.x), i1 = ex2k(bm.y - b.y);
+          uint32_t h, l;
+          split2(kf.x * e0, kf.y * e1, h, l);
+          *reinterpret_cast<uint32_t *>(sm + SM::kPl + SM::PL_AH + kmajor64_off(r, kc)) = h;
+          *reinterpret_cast<uint32_t *>(sm + SM::kPl + SM::PL_AL + kmajor64_off(r, kc)) = l;
+          split2(qf.x * e0, qf.y * e1, h, l);
+          *reinterpret_cast<uint32_t *>(sm + SM::kPl + SM::PL_AH + kmajor64_off(32 + r, kc)) = h;
+          *reinterpret_cast<uint32_t *>(sm + SM::kPl + SM::PL_AL + kmajor64_off(32 + r, kc)) = l;
+          split2(kf.x * i0, kf.y * i1, h, l);
+          *reinterpret_cast<uint32_t *>(sm + SM::kPl + SM::PL_BH + kmajor64_off(r, kc)) = h;
+          *reinterpret_cast<uint32_t *>(sm + SM::kPl + SM::PL_BL + kmajor64_off(r, kc)) = l;
+          kg0 = kf.x * e0 * ebm0; kg1 = kf.y * e1 * ebm1;
+          qg0 = a.scale * qf.x * e0 * ebm0; qg1 = a.scale * qf.y * e1 * ebm1;
+          kt0 = kf.x * i0 * elt0; kt1 = kf.y * i1 * elt1;
+        } else {
+          const float eb0 = ex2k(b.x), eb1 = ex2k(b.y);
+          kg0 = kf.x * eb0; kg1 = kf.y * eb1;
+          qg0 = a.scale * qf.x * eb0; qg1 = a.scale * qf.y * eb1;
+          kt0 = kf.x * ex2k(bl.x - b.x); kt1 = kf.y * ex2k(bl.y - b.y);
+        }
+        const __half2 kg = __floats2half2_rn(kg0, kg1), qg = __floats2half2_rn(qg0, qg1);
+        *reinterpret_cast<__half2 *>(kqi + p * kKqPanel + off) = kg;
+        *reinterpret_cast<__half2 *>(kqi + p * kKqPanel + kC * 128 + off) = qg;
+        *reinterpret_cast<__half2 *>(sm + SM::kKt + p * C * 128 + off) = __floats2half2_rn(kt0, kt1);
+      }
+      if (!wide) {
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (tid == 0) {
+          // [K~; Q~] K^^T over the half panel's 32 channels (M = 128: rows 64..
+          // are not read back), hi hi + lo hi + hi lo
+          constexpr uint32_t id = idesc_bf16(128, C, 0, 0);
+#pragma unroll
+          for (int k0 = 0; k0 < 32; k0 += 16) {
+            const uint64_t ah = make_desc_sw64(sPl + SM::PL_AH + k0 * 2, 512);
+            const uint64_t al = make_desc_sw64(sPl + SM::PL_AL + k0 * 2, 512);
+            const uint64_t bh = make_desc_sw64(sPl + SM::PL_BH + k0 * 2, 512);
+            const uint64_t bo = make_desc_sw64(sPl + SM::PL_BL + k0 * 2, 512);
+            mma_f16(tmem, ah, bh, id, (hp > 0 || k0 > 0) ? 1u : 0u);
+            mma_f16(tmem, al, bh, id, 1u);
+            mma_f16(tmem, ah, bo, id, 1u);
+          }
+          mma_commit(bar_mma);
+        }
+      }
+    }
+  } else
   {
     const int pp = tid & 31, rg = tid >> 5;  // channel pair, group of 8 rows
     const int col = 2 * pp;                  // first channel of the pair in the panel
@@ -280,7 +378,7 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   unsigned char *opAqk = sm + SM::kAqkOp;
   if (!wide) {
     // ---- A (lanes 0..31) and Aqk (lanes 32..63) from tensor memory ----
-    mbar_wait(bar_mma, (NP - 1) & 1, abort_flag);
+    mbar_wait(bar_mma, (SM::NH - 1) & 1, abort_flag);
     fence_after_sync();
     if (warp < 2) {
       uint32_t v[32];
@@ -431,7 +529,7 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     }
     mma_commit(bar_mma);
   }
-  mbar_wait(bar_mma, (wide ? 0 : NP) & 1, abort_flag);
+  mbar_wait(bar_mma, (wide ? 0 : SM::NH) & 1, abort_flag);
   fence_after_sync();
 
   // ---- the image [P1; AqkT], 32 columns per row in the 64-byte swizzle:
