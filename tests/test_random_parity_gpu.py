@@ -62,3 +62,21 @@ def test_random_recurrent(seed):
     og, hg = gpu_heads(o, hT)
     assert_close(og, o_ref, kind_of(c), f"{c} o")
     assert_close(hg, h_ref, kind_of(c), f"{c} hT")
+
+
+@pytest.mark.parametrize("seed", range(200, 216))
+def test_random_lockstep_bitwise(seed):
+    """The lockstep launch on random bf16 scalar-gate shapes (its head start
+    sized to each one) equals the split kernels bit for bit."""
+    c, lengths = draw_case(seed)
+    c = synth.Case(c.name, B=1, T=c.T, H=c.H, HV=c.HV, dk=c.dk, dv=c.dv, chunk=c.chunk,
+                   dtype=torch.bfloat16, gate_mode=0, gate_dist="uniform", gate_low=c.gate_low,
+                   h0_std=c.h0_std, n_seqs=c.n_seqs, seed=c.seed)
+    x = synth.make_inputs(c, lengths=lengths)
+    d = to_dev(x)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    o, hT = gdn.gdn_chunk_fwd(*args, scale=c.scale, chunk=c.chunk, cu_seqlens=d["cu_seqlens"])
+    o2, h2 = gdn.gdn_chunk_fwd_lockstep(*args, scale=c.scale, chunk=c.chunk,
+                                        cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(hT, h2), c.name
