@@ -80,3 +80,22 @@ def test_random_lockstep_bitwise(seed):
                                         cu_seqlens=d["cu_seqlens"])
     torch.cuda.synchronize()
     assert torch.equal(o, o2) and torch.equal(hT, h2), c.name
+
+
+@pytest.mark.parametrize("seed", range(300, 312))
+def test_random_per_key_chunk64(seed):
+    """The per-key gate (KDA) at chunk 64, which the draws above never pick:
+    the same shapes, dtypes and packed length mixes, against the oracle."""
+    c, lengths = draw_case(seed)
+    c = synth.Case(f"{c.name}_kda64", B=1, T=c.T, H=c.H, HV=c.HV, dk=c.dk, dv=c.dv, chunk=64,
+                   dtype=c.dtype, gate_mode=1, gate_dist="uniform", gate_low=c.gate_low,
+                   h0_std=c.h0_std, n_seqs=c.n_seqs, seed=c.seed)
+    x = synth.make_inputs(c, lengths=lengths)
+    d = to_dev(x)
+    o, hT = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], scale=c.scale,
+                              chunk=c.chunk, cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    o_ref, h_ref = run_oracle(c, x)
+    og, hg = gpu_heads(o, hT)
+    assert_close(og, o_ref, kind_of(c), f"{c} o")
+    assert_close(hg, h_ref, kind_of(c), f"{c} hT")
