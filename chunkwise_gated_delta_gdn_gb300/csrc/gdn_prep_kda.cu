@@ -2,8 +2,9 @@
 // path at chunk 32 (other chunk sizes run gdn_prep_tc.cu; both write the same
 // outputs for the scan kernel gdn_scan_tc.cu).
 //
-// One CTA (128 threads) per (chunk slot, value head), three per SM (about 65
-// KB of shared memory and 128 tensor-memory columns each).  The chunk's key,
+// One CTA (128 threads) per (chunk slot, value head), five per SM at dk = 128
+// (45 KB of shared memory, 80 registers and 64 tensor-memory columns each),
+// four at dk = 64.  The chunk's key,
 // query and gate tiles arrive by TMA.  The gates are summed along the chunk
 // per key channel, b_r = sum_{j <= r} g_j (log2 units here), and every
 // exponential of the chunk is taken against one reference row m = 16:
@@ -65,9 +66,9 @@ template <int DK>
 struct KdaSmem {
   static constexpr int NP = DK / 64;  // 64-channel panels
   // dk = 128 builds the factored planes per 32-channel half panel (64-byte
-  // swizzle, 12 KB) and puts the solve's fp32 T and scratch over the gate
-  // tile once it is dead, so that four CTAs share an SM; dk = 64 fits four
-  // with whole-panel planes
+  // swizzle, 12 KB) and puts the solve's fp32 T and scratch, and Kt, over the
+  // gate tile once it is dead, so that five CTAs share an SM; dk = 64 fits
+  // four with whole-panel planes
   static constexpr bool HALF = DK == 128;
   static constexpr int NH = HALF ? 2 * NP : NP;  // plane products per unit
   // TMA tiles: K and Q bf16 (C rows x 128 bytes per panel, 128-byte swizzle),
@@ -82,14 +83,21 @@ struct KdaSmem {
   static constexpr int ROWB = HALF ? 64 : 128;
   static constexpr int PL_AH = 0, PL_AL = 64 * ROWB, PL_BH = 128 * ROWB, PL_BL = 160 * ROWB;
   static constexpr int PLANES = 192 * ROWB;
-  // Kt as fp16 token rows, two 64-channel panels (P1's M = 128 reads both)
-  static constexpr int kKt = kPl + PLANES;
-  static constexpr int kBeta = kKt + 2 * kC * 128;
+  // Kt as fp16 token rows, two 64-channel panels (P1's M = 128 reads both).
+  // dk = 128: over the gate tile's second panel, written once the tile is
+  // dead (each thread holds its share in registers from the plane passes
+  // until then), so that five CTAs share an SM; dk = 64: after the planes
+  static constexpr int kKt = HALF ? kG + kC * 256 : kPl + PLANES;
+  static constexpr int kBeta = HALF ? kPl + PLANES : kKt + 2 * kC * 128;
   static constexpr int kBar = kBeta + kC * 4;  // TMA tiles, products
   static constexpr int kTslot = kBar + 16;
   static constexpr int kAbort = kTslot + 4;
   static constexpr int kMeta = kAbort + 4;
-  static constexpr int kBytes = kMeta + 16 + 1024;
+  // 1 KB of alignment slack, except at dk = 128, where the kernel checks
+  // that the dynamic shared memory it received is already 1 KB aligned
+  static constexpr int kSlack = HALF ? 0 : 1024;
+  static constexpr int kBytes = kMeta + 16 + kSlack;
+  static constexpr int kPerSm = HALF ? 5 : 4;  // CTAs per SM
   // once the A / Aqk products have read the planes, their region holds fp32 A
   // (and, on the strong-decay path, fp32 Aqk), then the fp16 T image (B
   // operand), then the output image; fp32 T and the solve's scratch lie over
@@ -106,22 +114,32 @@ struct KdaSmem {
   static constexpr int kImg = kPl;
   static constexpr int kAqkOp = kK;
   static_assert(kAqkF + ARR <= kPl + PLANES, "fp32 A and Aqk inside the plane region");
-  static_assert(!HALF || kRs + 16 * LDC * 4 <= kPl, "T and scratch inside the dead gate tile");
+  static_assert(!HALF || kRs + 16 * LDC * 4 <= kKt, "T and scratch below Kt in the dead gate tile");
+  static_assert(!HALF || kKt + 2 * kC * 128 <= kPl, "Kt inside the dead gate tile");
   static_assert(HALF || kAqkF + ARR <= kTimg, "fp32 arrays below the T image");
   static_assert(kTimg + kC * 128 <= kPl + PLANES, "T image inside the planes region");
   static_assert(kPrepImage32Bytes <= PLANES, "output image inside the planes region");
   static_assert(kPl - kK >= 16384, "the Aqk operand's 128-row span over the dead tiles");
   static_assert(kBar % 8 == 0 && kPl % 1024 == 0 && kKt % 1024 == 0, "alignment");
-  static_assert(4 * (kBytes + 1024) <= 232448, "four CTAs per SM");
+  // 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+  static_assert(kPerSm * (kBytes + 1024) <= 233472, "CTAs per SM");
 };
 
+// At most 80 registers a thread (the bound for six CTAs; shared memory allows
+// five): a prep CTA then also fits beside a scan CTA of gdn_scan_tc.cu
+// (55.3K + 10.2K of the SM's 64K registers), where batches in flight run one
+// batch's prep on the SMs another batch's scan holds.
 template <int DK>
-__global__ void __launch_bounds__(kNT, 4)
+__global__ void __launch_bounds__(kNT, 6)
 gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   using SM = KdaSmem<DK>;
   constexpr int NP = SM::NP, C = kC, LDC = SM::LDC;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  if (sm - smem_raw > SM::kSlack) {  // dynamic shared memory not aligned as needed
+    if (threadIdx.x == 0) atomicOr(a.flags, kFlagLaunchConfig);
+    return;
+  }
   float *Bs = reinterpret_cast<float *>(sm + SM::kBeta);
   int *meta = reinterpret_cast<int *>(sm + SM::kMeta);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SM::kTslot);
@@ -153,7 +171,9 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   const int t0 = meta[0], L = meta[1];
 
   // ---- set-up, tiles by TMA ----
-  constexpr uint32_t kTmemCols = 128;  // A / Aqk at 0, P1 at 32, Aqk T at 64
+  // A / Aqk at 0, then (once they are read out) P1 at 0 and Aqk T at 32: 64
+  // columns, so that five CTAs fit the SM's 512
+  constexpr uint32_t kTmemCols = 64;
   if (warp == 0) tmem_alloc(smem_addr(tslot), kTmemCols);
   if (tid == 0) {
     *abort_flag = 0;
@@ -209,13 +229,16 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
   // ---- one pass over the tile per 64-channel panel (dk = 64) or 32-channel
   //      half panel (dk = 128): factored planes (and their product), the
   //      gated image, Kt, the decays ----
+  // dk = 128: this thread's Kt values (half panel hp, row 4 rg + i, channel
+  // pair pp), held until the gate tile is dead
+  uint32_t ktr[SM::HALF ? SM::NH : 1][4];
   if constexpr (SM::HALF) {
     // 32-channel half panels hp: 16 channel pairs x 8 groups of 4 rows; the
     // planes in the 64-byte swizzle, one K = 32 product per half panel
     const int pp = tid & 15, rg = tid >> 4;
     unsigned char *kqi = a.kq_images + ((size_t)slot * a.HV + hv) * kq_image_bytes(DK);
     const uint32_t sPl = smem_addr(sm + SM::kPl);
-#pragma unroll 1
+#pragma unroll
     for (int hp = 0; hp < SM::NH; hp++) {
       const int p = hp >> 1, col = 32 * (hp & 1) + 2 * pp;  // first channel of the pair in the panel
       const int kc = col & 31;                                 // and in the half panel
@@ -231,7 +254,7 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       if (rg == 0)
         *reinterpret_cast<float2 *>(a.decays + ((size_t)slot * a.HV + hv) * DK + p * 64 + col) =
             make_float2(ex2k(bl.x), ex2k(bl.y));
-#pragma unroll 2
+#pragma unroll
       for (int i = 0; i < 4; i++) {
         const int r = 4 * rg + i;
         // element (r, col) of a 64-channel K-major row in the 128-byte swizzle,
@@ -266,7 +289,8 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
         const __half2 kg = __floats2half2_rn(kg0, kg1), qg = __floats2half2_rn(qg0, qg1);
         *reinterpret_cast<__half2 *>(kqi + p * kKqPanel + off) = kg;
         *reinterpret_cast<__half2 *>(kqi + p * kKqPanel + kC * 128 + off) = qg;
-        *reinterpret_cast<__half2 *>(sm + SM::kKt + p * C * 128 + off) = __floats2half2_rn(kt0, kt1);
+        const __half2 kt = __floats2half2_rn(kt0, kt1);
+        ktr[hp][i] = *reinterpret_cast<const uint32_t *>(&kt);
       }
       if (!wide) {
         fence_proxy_async();
@@ -458,6 +482,21 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
     }
   }
   __syncthreads();
+  if constexpr (SM::HALF) {
+    // every reader of the gate tile is done: Kt over its second panel
+    const int pp = tid & 15, rg = tid >> 4;
+#pragma unroll
+    for (int hp = 0; hp < SM::NH; hp++) {
+      const int p = hp >> 1, col = 32 * (hp & 1) + 2 * pp;
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const int r = 4 * rg + i;
+        const uint32_t off = r * 128 + ((((col >> 3) ^ (r & 7)) << 4) | ((col & 7) * 2));
+        *reinterpret_cast<uint32_t *>(sm + SM::kKt + p * C * 128 + off) = ktr[hp][i];
+      }
+    }
+    fence_proxy_async();
+  }
 
   // ---- T = (I + A)^-1 ----
   constexpr int NB = C / 16;
@@ -524,8 +563,8 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
 #pragma unroll
     for (int k0 = 0; k0 < C; k0 += 16) {
       const uint64_t bd = make_desc(sT + k0 * 2, 16, 1024);
-      mma_f16(tmem + 32, make_desc(sKt + k0 * 128, C * 128, 1024), bd, idP, k0 > 0 ? 1u : 0u);
-      mma_f16(tmem + 64, make_desc(sAqk + k0 * 2, 16, 1024), bd, idQ, k0 > 0 ? 1u : 0u);
+      mma_f16(tmem, make_desc(sKt + k0 * 128, C * 128, 1024), bd, idP, k0 > 0 ? 1u : 0u);
+      mma_f16(tmem + 32, make_desc(sAqk + k0 * 2, 16, 1024), bd, idQ, k0 > 0 ? 1u : 0u);
     }
     mma_commit(bar_mma);
   }
@@ -556,8 +595,8 @@ gdn_prep_kda_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps) {
       }
     };
     // tensor-memory loads are warp-wide: every lane of a warp loads
-    put_row(tid, tmem + lane_base + 32, warp * 32 < DK);
-    if (warp == 0) put_row(128 + tid, tmem + lane_base + 64, true);
+    put_row(tid, tmem + lane_base, warp * 32 < DK);
+    if (warp == 0) put_row(128 + tid, tmem + lane_base + 32, true);
   }
   fence_proxy_async();
   fence_before_sync();
