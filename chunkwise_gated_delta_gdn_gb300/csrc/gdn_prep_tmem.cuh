@@ -530,21 +530,20 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
 #pragma unroll
       for (int h = 0; h < 2; h++) {  // 32 columns at a time
         uint32_t v[32];
-        const bool load = have && 32 * h < C;
-        if (load) {
+        if (have && 32 * h < C) {
           tmem_ld32_nowait(taddr + 32 * h, v);
           tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i++) v[i] = 0u;
         }
 #pragma unroll
         for (int ch = 0; ch < 4; ch++) {
           uint4 pk;
           __half2 *hh = reinterpret_cast<__half2 *>(&pk);
 #pragma unroll
-          for (int i = 0; i < 4; i++) {
-            const float f0 = load ? __uint_as_float(v[ch * 8 + 2 * i]) : 0.f;
-            const float f1 = load ? __uint_as_float(v[ch * 8 + 2 * i + 1]) : 0.f;
-            hh[i] = __floats2half2_rn(f0, f1);
-          }
+          for (int i = 0; i < 4; i++)
+            hh[i] = __floats2half2_rn(__uint_as_float(v[ch * 8 + 2 * i]), __uint_as_float(v[ch * 8 + 2 * i + 1]));
           *reinterpret_cast<uint4 *>(dst + kmajor_off(row, 32 * h + ch * 8, 64)) = pk;
         }
       }
