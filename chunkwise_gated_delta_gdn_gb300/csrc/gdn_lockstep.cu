@@ -16,7 +16,7 @@
 // inputs, so the results equal gdn_chunk_fwd's bit for bit.  The prep has only
 // the SMs the scan leaves (one CTA per SM: the scan needs about 213 KB of
 // shared memory), three warpgroups each: fewer units in flight than the split
-// prep kernel's three CTAs on every SM.  So the prep gets a head start: the
+// prep kernel's four CTAs on every SM.  So the prep gets a head start: the
 // split prep kernel runs first over the first head_slots chunk slots on every
 // SM, setting their flags as well, and the lockstep's prep warpgroups take the
 // slots after them while the scan walks the chunks.
@@ -101,14 +101,14 @@ cudaError_t launch_one(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &m
   // finish the other units while the scan walks its chain; measured on this
   // GPU, one chunk step of the scan takes about kStepPerUnit of a prep unit
   // at three per SM (1.2 against 24 us).  The head start runs in whole waves
-  // of the split prep (n_sm x 3 CTAs at once), so its units are rounded up to
+  // of the split prep (n_sm x 4 CTAs at once), so its units are rounded up to
   // a wave and its slots down (a few more units in the next wave would cost a
   // whole unit's time).  At 32k tokens (H = 16, 96 scan blocks) this covers
   // half of the slots, at 4096 tokens 0.88 of them; the swept optima were 0.5
   // and 0.7-0.88.
   if (head_slots < 0) {
     constexpr double kStepPerUnit = 0.05;
-    constexpr long kPrepPerSm = 3;  // split prep CTAs per SM
+    constexpr long kPrepPerSm = 4;  // split prep CTAs per SM
     const long units = (long)pa.n_slots * pa.H;
     const long chain = pa.seq.cu ? ((long)pa.seq.Ttot + (long)C * pa.seq.n_seqs - 1) / ((long)C * pa.seq.n_seqs)
                                  : ((long)pa.seq.T + C - 1) / C;

@@ -1,10 +1,10 @@
 // gdn_prep_tmem.cu -- the chunk-prep kernel of the bf16 scalar-gate (GDN)
 // path: one CTA of 128 threads per (chunk slot, q/k head), running the unit of
-// gdn_prep_tmem.cuh.  Three CTAs share an SM (128 tensor-memory columns and
-// about 75 KB of shared memory each), so that their latency-bound phases
-// overlap.  Launched over every slot before the scan kernel, or over the first
-// slots only, publishing each unit's ready flag, ahead of the lockstep launch
-// (gdn_lockstep.cu).
+// gdn_prep_tmem.cuh.  Four CTAs share an SM (128 tensor-memory columns, about
+// 56 KB of shared memory and at most 128 registers a thread each), so that
+// their latency-bound phases overlap.  Launched over every slot before the
+// scan kernel, or over the first slots only, publishing each unit's ready
+// flag, ahead of the lockstep launch (gdn_lockstep.cu).
 #include "gdn_prep_tmem.cuh"
 
 namespace gdn {
@@ -13,7 +13,7 @@ namespace {
 using namespace sm100;
 
 template <int C, int DK>
-__global__ void __launch_bounds__(128, 3)
+__global__ void __launch_bounds__(128, 4)
 gdn_prep_tmem_kernel(const PrepArgs a, const __grid_constant__ ScanMaps maps, int *ready) {
   extern __shared__ unsigned char smem_raw[];
   // 1 KB-aligned base, as an offset into the shared array (the compiler then
@@ -43,7 +43,7 @@ cudaError_t launch_one(const PrepArgs &a, const ScanMaps &maps, int n_slots, int
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
   if (err != cudaSuccess) return err;
-  // three CTAs per SM need the largest shared-memory carve-out
+  // four CTAs per SM need the largest shared-memory carve-out
   err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (err != cudaSuccess) return err;
   kern<<<dim3(n_slots, a.H), 128, SM::kBytes, stream>>>(a, maps, ready);

@@ -61,28 +61,29 @@ __device__ __forceinline__ float ex2(float x) {
 
 template <int C>
 struct PrepTmemSmem {
-  static constexpr int LDT = C + 4;               // fp32 row stride of A^T / T^T
-  // [K; Q; K_next], K-major, always two panels of 192 rows x 128 bytes
+  static constexpr int LDT = 68;                    // fp32 row stride of A^T / T^T
+  // [K; Q; K_next] of each 64-column panel of the key/query dimension,
+  // K-major, 192 rows x 128 bytes; two panels (room for dk = 128), PSTR apart
   static constexpr int PANEL = 192 * 128;
-  static constexpr int KQ = 2 * PANEL;
-  // Each panel's query rows (64..127) are free once the Gram has read them
-  // and the [K_next; Q] image has been stored: panel 0's hold the W scratch of
-  // the solve, then T as a K-major B operand, then the staged E rows; panel
-  // 1's hold D T.
-  static constexpr int QS0 = 64 * 128;
-  static constexpr int QS1 = PANEL + 64 * 128;
+  static constexpr int PSTR = PANEL + 1024;
   static constexpr int kKQ = 0;
-  static constexpr int kWG = KQ;
-  // per value head, reused in turn
-  static constexpr int WG_AQK = 0;                // Aqk, K-major, 64 rows (8 KB); then AqkT staged
-  static constexpr int WG_A = 8 * 1024;           // A^T -> T^T, fp32, row stride LDT; then P1 staged
-  static constexpr int A_BYTES = ((C * LDT * 4 > 16384 ? C * LDT * 4 : 16384) + 1023) / 1024 * 1024;
-  static constexpr int WG_G = WG_A + A_BYTES;     // cumulative gates (log2 units)
-  static constexpr int WG_BETA = WG_G + C * 4;
-  static constexpr int WG_DEC = WG_BETA + C * 4;
-  static constexpr int WG_WF = WG_DEC + C * 4;    // cross-block decay factors (32)
-  static constexpr int WG_BYTES = WG_WF + 32 * 4;
-  static constexpr int kBar = kWG + WG_BYTES;     // tma, gram, mma
+  // Once both Gram products have read the query and next-key rows and the
+  // [K_next; Q] image has been stored, those rows hold the per-head buffers:
+  //   X2  panel 0's rows 64..191 and the 1 KB after them: A^T, then T^T, in
+  //       fp32 (row stride LDT), then the fp16 T and D T images (8 KB each),
+  //       then the staged Aqk T rows (over T), then the staged P1 rows
+  //   AG  panel 1's rows 64..191: the fp16 Aqk image (later the staged E
+  //       rows), then the image of Gn = K_next K^T; read together as one
+  //       128-row operand
+  static constexpr int kX2 = 64 * 128;
+  static constexpr int kAG = PSTR + 64 * 128;
+  static constexpr int kGn = kAG + 64 * 128;
+  static constexpr int kW = PSTR + PANEL;           // W scratch of the solve
+  static constexpr int kG = kW + 4 * 32 * 9 * 4;    // cumulative gates (log2 units)
+  static constexpr int kBeta = kG + C * 4;
+  static constexpr int kDec = kBeta + C * 4;
+  static constexpr int kWf = kDec + C * 4;          // cross-block decay factors (32)
+  static constexpr int kBar = kWf + 32 * 4;         // tma, gram, mma
   static constexpr int kMisc = kBar + 3 * 8;
   // a CTA running one unit at a time: the layout plus 1 KB of alignment
   // slack; a CTA of several warpgroups gives each a slice of kSlice bytes (a
@@ -90,9 +91,10 @@ struct PrepTmemSmem {
   // to the caller (its tensor-memory address slot).
   static constexpr int kBytes = kMisc + 32 + 1024;
   static constexpr int kSlice = (kMisc + 32 + 1023) / 1024 * 1024;
+  static_assert(C * LDT * 4 <= PSTR - kX2, "A^T in X2");
   static_assert(kBar % 8 == 0, "mbarrier alignment");
-  static_assert(32 * 9 * 4 * 4 <= 8192, "W scratch in panel 0's query rows");
-  static_assert(kBytes <= 232448, "shared memory of one CTA");
+  // four CTAs per SM: 228 KB of shared memory, 1 KB of it reserved per CTA
+  static_assert(4 * (kBytes + 1024) <= 233472, "four CTAs per SM");
 };
 
 // Completions seen so far of the three mbarriers of a warpgroup's slice (the
@@ -164,11 +166,12 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
   if (!meta[2]) return;  // unused slot: the scan never reads it
   const int t0 = meta[0], L = meta[1], Ln = meta[3];
 
-  // Gram (C columns) at 0, then P1, Aqk T and E in turn at 64
+  // Gram (C columns) at 0; Gn, then Aqk T, E and P1 in turn, at 64
   if (C < 64) {  // zero the rows no TMA box covers
-    for (int i = tid; i < SM::KQ / 16; i += NT) {
-      const int row = (i * 16 % SM::PANEL) / 128;
-      if ((row & 63) >= C) reinterpret_cast<uint4 *>(kq)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < 2 * SM::PANEL / 16; i += NT) {
+      const int p = i / (SM::PANEL / 16), w = i % (SM::PANEL / 16);
+      if (((w / 8) & 63) >= C)
+        *reinterpret_cast<uint4 *>(kq + p * SM::PSTR + w * 16) = make_uint4(0, 0, 0, 0);
     }
   }
   fence_proxy_async();
@@ -176,9 +179,9 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
     mbar_arrive_expect_tx(bar_tma, (Ln > 0 ? 3 : 2) * C * DK * 2);
 #pragma unroll
     for (int p = 0; p < DK / 64; p++) {
-      tma_load_3d(smem_addr(kq + p * SM::PANEL), &maps.k, p * 64, hq, t0, bar_tma);
-      tma_load_3d(smem_addr(kq + p * SM::PANEL + 64 * 128), &maps.q, p * 64, hq, t0, bar_tma);
-      if (Ln > 0) tma_load_3d(smem_addr(kq + p * SM::PANEL + 128 * 128), &maps.k, p * 64, hq, t0 + C, bar_tma);
+      tma_load_3d(smem_addr(kq + p * SM::PSTR), &maps.k, p * 64, hq, t0, bar_tma);
+      tma_load_3d(smem_addr(kq + p * SM::PSTR + 64 * 128), &maps.q, p * 64, hq, t0, bar_tma);
+      if (Ln > 0) tma_load_3d(smem_addr(kq + p * SM::PSTR + 128 * 128), &maps.k, p * 64, hq, t0 + C, bar_tma);
     }
   }
   // value head j's raw gates and beta by cp.async (zeros past the chunk's
@@ -188,8 +191,8 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
   // products run.  Thread t copies and later reads only its own row.
   const int t = tid;
   const int G = a.HV / a.H;
-  float *raw_g = reinterpret_cast<float *>(sm + SM::kWG + SM::WG_DEC);
-  float *raw_b = reinterpret_cast<float *>(sm + SM::kWG + SM::WG_BETA);
+  float *raw_g = reinterpret_cast<float *>(sm + SM::kDec);
+  float *raw_b = reinterpret_cast<float *>(sm + SM::kBeta);
   auto fetch = [&](int j) {
     if (t < C && j < G) {
       const bool in = t < L;
@@ -217,7 +220,7 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
         const int idx = tid + (b0 + u) * NT;
         const int p = idx / (3 * C * 8), rem = idx % (3 * C * 8);
         const int third = rem / (C * 8), r = (rem / 8) % C, chunk = rem % 8;
-        ptr[u] = reinterpret_cast<uint4 *>(kq + p * SM::PANEL + (third * 64 + r) * 128 + chunk * 16);
+        ptr[u] = reinterpret_cast<uint4 *>(kq + p * SM::PSTR + (third * 64 + r) * 128 + chunk * 16);
         keep[u] = r < (third == 2 ? Ln : L);
         v[u] = keep[u] ? *ptr[u] : make_uint4(0, 0, 0, 0);
       }
@@ -241,14 +244,18 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
   fence_before_sync();
   named_bar(bar_id, 128);
   fence_after_sync();
-  // ---- G = [K; Q] K^T (columns [0, C)) ----
+  // ---- G = [K; Q] K^T (columns [0, C)) and [Q; K_next] K^T (columns
+  //      [64, 64 + C)), whose lanes 64.. hold Gn = K_next K^T ----
+  const uint32_t tX = tmem + 64;  // Gn, then Aqk T, E and P1 in turn
   if (tid == 0) {
     const uint32_t sKQ = smem_addr(kq);
     constexpr uint32_t id = idesc_f16(128, C, 0, 0);
 #pragma unroll
     for (int k0 = 0; k0 < DK; k0 += 16) {
-      const uint64_t d = make_desc(sKQ + (k0 >> 6) * SM::PANEL + (k0 & 63) * 2, 16, 1024);
-      mma_f16(tmem, d, d, id, k0 > 0 ? 1u : 0u);  // B = the key rows of the same image
+      const uint32_t base = sKQ + (k0 >> 6) * SM::PSTR + (k0 & 63) * 2;
+      const uint64_t d = make_desc(base, 16, 1024);  // [K; Q], and its key rows as B
+      mma_f16(tmem, d, d, id, k0 > 0 ? 1u : 0u);
+      mma_f16(tX, make_desc(base + 64 * 128, 16, 1024), d, id, k0 > 0 ? 1u : 0u);
     }
     mma_commit(bar_gram);
   }
@@ -258,24 +265,48 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
     unsigned char *dst = a.kq_images + ((size_t)slot * a.H + hq) * kq_image_bytes(DK);
 #pragma unroll
     for (int p = 0; p < DK / 64; p++) {
-      bulk_s2g(dst + p * 16384, smem_addr(kq + p * SM::PANEL + 16384), 8192);
-      bulk_s2g(dst + p * 16384 + 8192, smem_addr(kq + p * SM::PANEL + 8192), 8192);
+      bulk_s2g(dst + p * 16384, smem_addr(kq + p * SM::PSTR + 16384), 8192);
+      bulk_s2g(dst + p * 16384 + 8192, smem_addr(kq + p * SM::PSTR + 8192), 8192);
     }
     bulk_commit();
   }
 
+  // this lane's row at `taddr` -> row `row` of a 64-column K-major fp16
+  // image at `dst` (zeros when !have)
+  auto put_row = [&](unsigned char *dst, int row, uint32_t taddr, bool have) {
+#pragma unroll
+    for (int h = 0; h < 2; h++) {  // 32 columns at a time
+      uint32_t v[32];
+      if (have && 32 * h < C) {
+        tmem_ld32_nowait(taddr + 32 * h, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i++) v[i] = 0u;
+      }
+#pragma unroll
+      for (int ch = 0; ch < 4; ch++) {
+        uint4 pk;
+        __half2 *hh = reinterpret_cast<__half2 *>(&pk);
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+          hh[i] = __floats2half2_rn(__uint_as_float(v[ch * 8 + 2 * i]), __uint_as_float(v[ch * 8 + 2 * i + 1]));
+        *reinterpret_cast<uint4 *>(dst + kmajor_off(row, 32 * h + ch * 8, 64)) = pk;
+      }
+    }
+  };
+
   // ---- per value head ----
-  unsigned char *ws = sm + SM::kWG;
-  float *As = reinterpret_cast<float *>(ws + SM::WG_A);
-  float *Rs = reinterpret_cast<float *>(sm + SM::QS0);  // W scratch of the solve
-  float *Gs = reinterpret_cast<float *>(ws + SM::WG_G);
-  float *Bs = reinterpret_cast<float *>(ws + SM::WG_BETA);
-  float *Ds = reinterpret_cast<float *>(ws + SM::WG_DEC);
+  float *As = reinterpret_cast<float *>(sm + SM::kX2);
+  float *Rs = reinterpret_cast<float *>(sm + SM::kW);  // W scratch of the solve
+  float *Gs = reinterpret_cast<float *>(sm + SM::kG);
+  float *Bs = reinterpret_cast<float *>(sm + SM::kBeta);
+  float *Ds = reinterpret_cast<float *>(sm + SM::kDec);
   const uint32_t bar_mma = bar_tma + 16;
-  const uint32_t tX = tmem + 64;  // P1, then Aqk T, then E
   const int wlane0 = (warp & 3) * 32;  // first tensor-memory lane of this warp
+  const uint32_t sKQ = smem_addr(kq), sX2 = smem_addr(sm + SM::kX2), sAG = smem_addr(sm + SM::kAG);
   bool first = true;
-  float *Wf = reinterpret_cast<float *>(ws + SM::WG_WF);  // exp2(b_32 - b_s), s < 32
+  float *Wf = reinterpret_cast<float *>(sm + SM::kWf);  // exp2(b_32 - b_s), s < 32
   for (int j = 0; j < G; j++) {
     const int hv = hq * G + j;
     // the previous head's image stores must have read the buffers reused below
@@ -308,12 +339,17 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
       if (lane + 32 < C) { Gs[lane + 32] = x1; Ds[lane + 32] = ex2(blast - x1); }
       if (C > 32) Wf[lane] = ex2(__shfl_sync(0xffffffffu, x1, 0) - x0);
     }
-    named_bar(bar_id, 128);
     if (first) {
+      // the Gram products are done, and the [K_next; Q] image store has read
+      // the rows that the per-head buffers reuse; Gn's rows -> its image
       mbar_wait(bar_gram, ph.gram++ & 1, abort_flag);
+      if (t == 0) bulk_wait_read_all();
+      named_bar(bar_id, 128);
       fence_after_sync();
+      if (t >= 64) put_row(sm + SM::kGn, t - 64, tX + lane_base, wlane0 - 64 < C);
       first = false;
     }
+    named_bar(bar_id, 128);
 
     // ---- A (key lanes) and Aqk (query lanes) from the shared Gram ----
     // decay of column s for row r in 32-row block o: direct inside the block,
@@ -359,17 +395,20 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
       const int r = t - 64, o = wlane0 - 64;
       const float br = Gs[r];
       const float su = o > 0 ? a.scale * ex2(br - Gs[o]) : 0.f;
-      unsigned char *aq = ws + SM::WG_AQK;
+      unsigned char *aq = sm + SM::kAG;
 #pragma unroll
       for (int h = 0; h < C / 32; h++) {
-        uint32_t g[32];
-        const bool any = 32 * h <= o;
-        if (any) {
-          tmem_ld32_nowait(tmem + lane_base + 32 * h, g);
-          tmem_wait_ld();
+        if (32 * h > o) {  // s > r throughout: a zero block of Aqk
+#pragma unroll
+          for (int ch = 0; ch < 4; ch++)
+            *reinterpret_cast<uint4 *>(aq + kmajor_off(r, 32 * h + ch * 8, 64)) = make_uint4(0, 0, 0, 0);
+          continue;
         }
+        uint32_t g[32];
+        tmem_ld32_nowait(tmem + lane_base + 32 * h, g);
+        tmem_wait_ld();
         float fv[32];
-        if (any) {
+        {
           const float *src = 32 * h < o ? Wf : Gs + 32 * h;
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
@@ -385,11 +424,11 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
           for (int i = 0; i < 4; i++) {
             const int s = 32 * h + ch * 8 + 2 * i;
             const int ii = ch * 8 + 2 * i;
-            float v0 = 0.f, v1 = 0.f;
+            float v0, v1;
             if (32 * h < o) {
               v0 = su * __uint_as_float(g[ii]) * fv[ii];
               v1 = su * __uint_as_float(g[ii + 1]) * fv[ii + 1];
-            } else if (any) {
+            } else {
               v0 = s <= r ? a.scale * __uint_as_float(g[ii]) * ex2(br - fv[ii]) : 0.f;
               v1 = s + 1 <= r ? a.scale * __uint_as_float(g[ii + 1]) * ex2(br - fv[ii + 1]) : 0.f;
             }
@@ -403,9 +442,6 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
     named_bar(bar_id, 128);
 
     // ---- T = (I + A)^-1, transposed in place: As[j * LDT + r] = T[r][j] ----
-    // (the [K_next; Q] image store must have read the query rows that hold
-    // the W scratch from here on)
-    if (j == 0 && t == 0) bulk_wait_read_all();
     // (1) 16 x 16 diagonal blocks: warp w, lanes 0..15 = columns, rows in
     //     registers, forward substitution in fp32
     {
@@ -498,24 +534,35 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
       }
     }
 
-    // ---- fp16 images of T and D T as K-major B operands: row j = T[.][j];
-    //      one 16-byte chunk per task, spread over the whole warpgroup ----
-    for (int task = t; task < C * (C / 8); task += NT) {
-      const int j = task % C, ch = task / C;
-      const float *trow = As + j * LDT;
-      const float4 t0v = *reinterpret_cast<const float4 *>(trow + ch * 8);
-      const float4 t1v = *reinterpret_cast<const float4 *>(trow + ch * 8 + 4);
-      const float4 d0 = *reinterpret_cast<const float4 *>(Ds + ch * 8);
-      const float4 d1 = *reinterpret_cast<const float4 *>(Ds + ch * 8 + 4);
-      uint4 pt, pd;
-      __half2 *ht = reinterpret_cast<__half2 *>(&pt);
-      __half2 *hd = reinterpret_cast<__half2 *>(&pd);
-      ht[0] = __floats2half2_rn(t0v.x, t0v.y); ht[1] = __floats2half2_rn(t0v.z, t0v.w);
-      ht[2] = __floats2half2_rn(t1v.x, t1v.y); ht[3] = __floats2half2_rn(t1v.z, t1v.w);
-      hd[0] = __floats2half2_rn(d0.x * t0v.x, d0.y * t0v.y); hd[1] = __floats2half2_rn(d0.z * t0v.z, d0.w * t0v.w);
-      hd[2] = __floats2half2_rn(d1.x * t1v.x, d1.y * t1v.y); hd[3] = __floats2half2_rn(d1.z * t1v.z, d1.w * t1v.w);
-      *reinterpret_cast<uint4 *>(sm + SM::QS0 + kmajor_off(j, ch * 8, 64)) = pt;
-      *reinterpret_cast<uint4 *>(sm + SM::QS1 + kmajor_off(j, ch * 8, 64)) = pd;
+    // ---- fp16 images of T and D T as K-major B operands (row j = T[.][j]),
+    //      over T^T's own space: every thread reads its 16-byte chunks, then
+    //      all write ----
+    {
+      constexpr int NU = C * (C / 8) / NT;
+      static_assert(C * (C / 8) % NT == 0, "image build tiling");
+      uint4 pt[NU], pd[NU];
+#pragma unroll
+      for (int u = 0; u < NU; u++) {
+        const int task = t + u * NT, jj = task % C, ch = task / C;
+        const float *trow = As + jj * LDT;
+        const float4 t0v = *reinterpret_cast<const float4 *>(trow + ch * 8);
+        const float4 t1v = *reinterpret_cast<const float4 *>(trow + ch * 8 + 4);
+        const float4 d0 = *reinterpret_cast<const float4 *>(Ds + ch * 8);
+        const float4 d1 = *reinterpret_cast<const float4 *>(Ds + ch * 8 + 4);
+        __half2 *ht = reinterpret_cast<__half2 *>(&pt[u]);
+        __half2 *hd = reinterpret_cast<__half2 *>(&pd[u]);
+        ht[0] = __floats2half2_rn(t0v.x, t0v.y); ht[1] = __floats2half2_rn(t0v.z, t0v.w);
+        ht[2] = __floats2half2_rn(t1v.x, t1v.y); ht[3] = __floats2half2_rn(t1v.z, t1v.w);
+        hd[0] = __floats2half2_rn(d0.x * t0v.x, d0.y * t0v.y); hd[1] = __floats2half2_rn(d0.z * t0v.z, d0.w * t0v.w);
+        hd[2] = __floats2half2_rn(d1.x * t1v.x, d1.y * t1v.y); hd[3] = __floats2half2_rn(d1.z * t1v.z, d1.w * t1v.w);
+      }
+      named_bar(bar_id, 128);
+#pragma unroll
+      for (int u = 0; u < NU; u++) {
+        const int task = t + u * NT, jj = task % C, ch = task / C;
+        *reinterpret_cast<uint4 *>(sm + SM::kX2 + kmajor_off(jj, ch * 8, 64)) = pt[u];
+        *reinterpret_cast<uint4 *>(sm + SM::kX2 + 8192 + kmajor_off(jj, ch * 8, 64)) = pd[u];
+      }
     }
     fence_proxy_async();
     fence_before_sync();
@@ -524,98 +571,71 @@ __device__ __forceinline__ void prep_tmem_unit(const PrepArgs &a, const ScanMaps
     // the decays and beta of this head are consumed: the next head's gates
     fetch(j + 1);
 
-    // this lane's row at `taddr` -> row `row` of a 64-column K-major fp16
-    // image at `dst` (zeros when !have)
-    auto put_row = [&](unsigned char *dst, int row, uint32_t taddr, bool have) {
-#pragma unroll
-      for (int h = 0; h < 2; h++) {  // 32 columns at a time
-        uint32_t v[32];
-        if (have && 32 * h < C) {
-          tmem_ld32_nowait(taddr + 32 * h, v);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; i++) v[i] = 0u;
-        }
-#pragma unroll
-        for (int ch = 0; ch < 4; ch++) {
-          uint4 pk;
-          __half2 *hh = reinterpret_cast<__half2 *>(&pk);
-#pragma unroll
-          for (int i = 0; i < 4; i++)
-            hh[i] = __floats2half2_rn(__uint_as_float(v[ch * 8 + 2 * i]), __uint_as_float(v[ch * 8 + 2 * i + 1]));
-          *reinterpret_cast<uint4 *>(dst + kmajor_off(row, 32 * h + ch * 8, 64)) = pk;
-        }
-      }
-    };
-    // staging of the image, over buffers dead by then: P1 (rows 0..127) over
-    // A^T, E (rows 128..191) over the T image, Aqk T (rows 192..255) over Aqk
-    unsigned char *stP1 = ws + SM::WG_A, *stE = sm + SM::QS0, *stAT = ws + SM::WG_AQK;
-    const uint32_t sKQ = smem_addr(kq);
-
-    // ---- P1 = K^T (D T) ----
+    // The image of this (chunk, value head): rows 0..127 = P1, 128..191 = E,
+    // 192..255 = Aqk T.  [Aqk; Gn] is the A operand of both Aqk T (output
+    // rows 0..63) and E = Gn (D T) (output rows 64..127).
+    unsigned char *dst = reinterpret_cast<unsigned char *>(a.tiles) + ((size_t)slot * a.HV + hv) * kLaImageBytes;
+    constexpr uint32_t idK = idesc_f16(128, C, 0, 0);
+    // ---- Aqk T, staged over the T image ----
     if (t == 0) {
-      const uint32_t sDT = smem_addr(sm + SM::QS1);
-      constexpr uint32_t idP = idesc_f16(128, C, 1, 0);  // A MN-major: keys read as K^T
 #pragma unroll
-      for (int k0 = 0; k0 < C; k0 += 16) {
-        mma_f16(tX, make_desc(sKQ + k0 * 128, SM::PANEL, 1024),
-                make_desc(sDT + k0 * 2, 16, 1024), idP, k0 > 0 ? 1u : 0u);
-      }
+      for (int k0 = 0; k0 < C; k0 += 16)
+        mma_f16(tX, make_desc(sAG + k0 * 2, 16, 1024), make_desc(sX2 + k0 * 2, 16, 1024), idK,
+                k0 > 0 ? 1u : 0u);
       mma_commit(bar_mma);
     }
     mbar_wait(bar_mma, ph.mma++ & 1, abort_flag);
     fence_after_sync();
-    put_row(stP1, t, tX + lane_base, wlane0 < DK);
+    if (t < 64) put_row(sm + SM::kX2, t, tX + lane_base, wlane0 < C);
     fence_proxy_async();
     fence_before_sync();
     named_bar(bar_id, 128);
     fence_after_sync();
-
-    // ---- AqkT = Aqk T ----
+    // ---- E = Gn (D T), staged over the Aqk image (zero for the last chunk
+    //      of a sequence) ----
     if (t == 0) {
-      const uint32_t sAqk = smem_addr(ws + SM::WG_AQK), sT = smem_addr(sm + SM::QS0);
-      constexpr uint32_t idQ = idesc_f16(128, C, 0, 0);
+      bulk_s2g(dst + 192 * 128, sX2, 64 * 128);
+      bulk_commit();
+      if (Ln > 0) {
 #pragma unroll
-      for (int k0 = 0; k0 < C; k0 += 16) {
-        mma_f16(tX, make_desc(sAqk + k0 * 2, 16, 1024),
-                make_desc(sT + k0 * 2, 16, 1024), idQ, k0 > 0 ? 1u : 0u);
-      }
-      mma_commit(bar_mma);
-    }
-    mbar_wait(bar_mma, ph.mma++ & 1, abort_flag);
-    fence_after_sync();
-    if (t < 64) put_row(stAT, t, tX + lane_base, wlane0 < C);
-    fence_proxy_async();
-    fence_before_sync();
-    named_bar(bar_id, 128);
-    fence_after_sync();
-
-    // ---- E = K_next P1 (M = 128 rows from the next-key tile, N = C, K = dk) ----
-    if (Ln > 0) {
-      if (t == 0) {
-        const uint32_t sKn = sKQ + 128 * 128, sP1 = smem_addr(stP1);
-        constexpr uint32_t idE = idesc_f16(128, C, 0, 1);
-#pragma unroll
-        for (int k0 = 0; k0 < DK; k0 += 16) {
-          mma_f16(tX, make_desc(sKn + (k0 >> 6) * SM::PANEL + (k0 & 63) * 2, 16, 1024),
-                  make_desc(sP1 + (k0 >> 4) * 2048, (DK / 8) * 1024, 1024), idE, k0 > 0 ? 1u : 0u);
-        }
+        for (int k0 = 0; k0 < C; k0 += 16)
+          mma_f16(tX, make_desc(sAG + k0 * 2, 16, 1024), make_desc(sX2 + 8192 + k0 * 2, 16, 1024),
+                  idK, k0 > 0 ? 1u : 0u);
         mma_commit(bar_mma);
       }
+    }
+    if (Ln > 0) {
       mbar_wait(bar_mma, ph.mma++ & 1, abort_flag);
       fence_after_sync();
     }
-    if (t < 64) put_row(stE, t, tX + lane_base, Ln > 0 && wlane0 < C);
+    if (t >= 64) put_row(sm + SM::kAG, t - 64, tX + lane_base, Ln > 0 && wlane0 - 64 < C);
+    fence_proxy_async();
+    fence_before_sync();
+    named_bar(bar_id, 128);
+    fence_after_sync();
+    // ---- P1 = K^T (D T), the key tile read MN-major, staged over X2 ----
+    if (t == 0) {
+      bulk_s2g(dst + 128 * 128, sAG, 64 * 128);
+      bulk_commit();
+      constexpr uint32_t idP = idesc_f16(128, C, 1, 0);
+#pragma unroll
+      for (int k0 = 0; k0 < C; k0 += 16)
+        mma_f16(tX, make_desc(sKQ + k0 * 128, SM::PSTR, 1024), make_desc(sX2 + 8192 + k0 * 2, 16, 1024),
+                idP, k0 > 0 ? 1u : 0u);
+      mma_commit(bar_mma);
+    }
+    mbar_wait(bar_mma, ph.mma++ & 1, abort_flag);
+    if (t == 0) bulk_wait_read_1();  // the staged Aqk T rows have been read
+    fence_before_sync();
+    named_bar(bar_id, 128);
+    fence_after_sync();
+    put_row(sm + SM::kX2, t, tX + lane_base, wlane0 < DK);
     fence_proxy_async();
     fence_before_sync();
     named_bar(bar_id, 128);
     fence_after_sync();
     if (t == 0) {
-      unsigned char *dst = reinterpret_cast<unsigned char *>(a.tiles) + ((size_t)slot * a.HV + hv) * kLaImageBytes;
-      bulk_s2g(dst, smem_addr(stP1), 128 * 128);
-      bulk_s2g(dst + 128 * 128, smem_addr(stE), 64 * 128);
-      bulk_s2g(dst + 192 * 128, smem_addr(stAT), 64 * 128);
+      bulk_s2g(dst, sX2, 128 * 128);
       bulk_commit();
     }
   }
