@@ -104,8 +104,8 @@ cudaError_t launch_one(const PrepArgs &pa, const ScanArgs &sa, const ScanMaps &m
   // of the split prep (n_sm x 4 CTAs at once), so its units are rounded up to
   // a wave and its slots down (a few more units in the next wave would cost a
   // whole unit's time).  At 32k tokens (H = 16, 96 scan blocks) this covers
-  // half of the slots, at 4096 tokens 0.88 of them; the swept optima were 0.5
-  // and 0.7-0.88.
+  // 0.52 of the slots, at 4096 tokens 0.59 of them; swept from 0.025 to 0.1,
+  // 0.05 is the best from 8192 tokens up.
   if (head_slots < 0) {
     constexpr double kStepPerUnit = 0.05;
     constexpr long kPrepPerSm = 4;  // split prep CTAs per SM

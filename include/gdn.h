@@ -182,12 +182,13 @@ GDN_API gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
  * first chunk slots on every SM (half of them at 32k tokens, more for shorter
  * inputs: enough that the prep warpgroups can finish the rest while the scan
  * walks its chunks), enqueued just before the cooperative launch.  A call that
- * must finish before the next work starts is faster this way (measured from
- * 2048 tokens up: 0.88 ms against 1.04 ms for gdn_chunk_fwd on 32k tokens, 16
- * q/k and 48 value heads of 128); independent calls in flight on several
- * streams are faster with gdn_chunk_fwd, whose kernels can share the GPU, while
- * cooperative launches run one at a time (PR #11223, "Notes for reviewers":
- * the composition is chosen by measurement).
+ * must finish before the next work starts is faster this way from about 8192
+ * tokens up (measured: 0.87 ms against 1.01 ms for gdn_chunk_fwd on 32k
+ * tokens, 16 q/k and 48 value heads of 128; at 2048 and 4096 tokens the two
+ * are within 3%); independent calls in flight on several streams are faster
+ * with gdn_chunk_fwd, whose kernels can share the GPU, while cooperative
+ * launches run one at a time (PR #11223, "Notes for reviewers": the
+ * composition is chosen by measurement).
  */
 GDN_API gdn_status gdn_chunk_fwd_lockstep(const void *q, const void *k, const void *v,
                               const float *g, const float *beta, const float *h0,
