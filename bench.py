@@ -63,7 +63,7 @@ def parse_args():
                     help="skip the lockstep launch's timing pass")
     ap.add_argument("--in-flight", type=int, default=3,
                     help="independent batches in flight in the throughput pass (3 measured "
-                         "best at 32k tokens: 2 / 3 / 4 give 38.3 / 40.3 / 39.1 M tokens/s)")
+                         "best at 32k tokens: 2 / 3 / 4 give 39.6 / 41.8 / 41.1 M tokens/s)")
     return ap.parse_args()
 
 
